@@ -1,0 +1,223 @@
+/*
+ * libhs -- HiSparse decode-time hot path on one GB300 (sm_103a).
+ *
+ * C ABI: plain pointers and sizes only.  Streams and events are passed as
+ * opaque `void*` holding a cudaStream_t / cudaEvent_t (NULL = legacy default
+ * stream).  Every device pointer named "device" must point to memory of the
+ * device the pool was created on.
+ *
+ * Sources.  Page "59188saintaubert.com ... HiSparse" (a summary of the
+ * HiSparse paper), section 02: two-level KV -- pinned host DRAM holds each
+ * active request's authoritative full KV, the GPU keeps a fixed hot buffer of
+ * B slots per request and layer, a page table maps each logical position to a
+ * cache slot or a host-only marker, LRU metadata drives replacement, and one
+ * fused RESOLVE kernel per sparse layer does hit detection, LRU replacement,
+ * metadata update and host fetch (logical index in, physical slot out).
+ * Page "GLM 5.3 Optimizations, Part 1: Hybrid HiSparse Offloading in vLLM",
+ * section "How it works": resident tokens are read in place and the tail is
+ * never evicted; hot tokens are read and their LRU entry refreshed; a miss
+ * copies a single row from pinned host memory into an LRU slot; hot pages are
+ * ordinary blocks of the same KV tensor, so the resolver hands out row ids
+ * that the sparse MLA kernel gathers with one stride; completed prefix pages
+ * are copied to host in one launch covering all sparse layers.
+ *
+ * Data layout (all owned by the pool unless stated):
+ *   KV row        row_elems bf16 values (576 = 512 latent + 64 rope)
+ *   kv_pool       device  bf16 [L][blocks_per_layer][P][row_elems]
+ *                 blocks 0 .. R*B/P-1 of every layer are the hot buffers:
+ *                 request r's hot slot s is block r*(B/P) + s/P, row s%P;
+ *                 blocks from R*B/P on hold resident pages
+ *   host_pool     pinned, mapped host bf16 [L][host_tokens][row_elems];
+ *                 request r's position p of layer l is row host_off[r] + p
+ *   row id        index of a row within one layer of kv_pool:
+ *                 block * P + offset (-1 = no row)
+ *   page_table    device int32 [R][max_pages]: block id, or -1 = host only
+ *   LRU metadata  device int32 [L][R][B] slot_pos (-1 = empty),
+ *                 slot_stamp (step of last use, -1 = never), lru_order (slots
+ *                 sorted by (stamp, slot) ascending)
+ *
+ * Errors.  Argument errors are returned synchronously.  Errors found on the
+ * device (bad indices in caller data) never trap: the kernel writes row id
+ * -1 for the offending entry and ORs a bit into the pool's device error word,
+ * which hs_check_errors() reads and clears.
+ */
+#ifndef HS_H
+#define HS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HS_OK = 0,
+  HS_ERR_INVALID = -1,  /* bad argument (null pointer, out-of-range index, bad shape) */
+  HS_ERR_CUDA = -2,     /* a CUDA runtime call failed */
+  HS_ERR_OOM = -3,      /* device or pinned host allocation failed */
+  HS_ERR_CAPACITY = -4, /* more misses than free slots were seen (error bit 4) */
+  HS_ERR_DEVICE = -5,   /* the device error word was non-zero */
+  HS_ERR_TIMEOUT = -6   /* a bounded wait gave up */
+} hs_status;
+
+/* Bits of the device error word (also returned by hs_check_errors). */
+#define HS_DEV_ERR_RANGE 1     /* selected position outside [0, ctx) and not -1 */
+#define HS_DEV_ERR_DUPLICATE 2 /* position repeated within one top-K row */
+#define HS_DEV_ERR_CAPACITY 4  /* misses exceeded the slots not used this step */
+#define HS_DEV_ERR_BLOCK 8     /* page table / row id names a block outside the pool */
+#define HS_DEV_ERR_WAIT 16     /* an in-kernel bounded wait gave up */
+
+typedef struct {
+  int32_t num_requests;    /* R */
+  int32_t num_layers;      /* L sparse layers */
+  int32_t top_k;           /* K: selections per (request, layer) and step */
+  int32_t hot_slots;       /* B: hot-buffer rows per (request, layer); multiple of page_tokens */
+  int32_t page_tokens;     /* P: tokens per page/block */
+  int32_t row_elems;       /* bf16 values per KV row; multiple of 8 (576 here) */
+  int32_t max_pages;       /* logical pages per request (page table width) */
+  int32_t reserved;        /* must be 0 */
+  int64_t host_tokens;     /* rows per layer in the pinned host pool */
+  int64_t resident_blocks; /* blocks per layer for resident pages (beyond the hot buffers) */
+} hs_pool_desc;
+
+typedef struct {
+  void* kv_pool;          /* device, see layout above */
+  void* host_pool;        /* host pointer of the pinned host pool */
+  void* host_pool_device; /* device-accessible alias of the same memory */
+  int32_t* page_table;    /* device [R][max_pages] */
+  int32_t* ctx_len;       /* device [R] */
+  int64_t* host_off;      /* device [R] */
+  int32_t* hot_block;     /* device [R][B/P] */
+  int32_t* slot_pos;      /* device [L][R][B] */
+  int32_t* slot_stamp;    /* device [L][R][B] */
+  int32_t* lru_order;     /* device [L][R][B] */
+  int32_t* step;          /* device scalar: the pool's decode-step counter */
+  int32_t* error_word;    /* device scalar */
+  int64_t blocks_per_layer;
+  int64_t kv_pool_bytes;
+  int64_t host_pool_bytes;
+} hs_pool_views;
+
+typedef struct hs_pool hs_pool; /* opaque, library-owned */
+
+/* Create a pool on the current CUDA device.  Allocates the pinned + mapped
+ * host pool (cudaHostAlloc), the per-layer GPU KV pool (hot-buffer blocks
+ * leased once per (request, layer), then resident blocks), the page table
+ * (all host-only), LRU metadata (all slots empty, stamp -1), the step counter
+ * (0) and the attention workspace.  Synchronous.  On failure *out is NULL and
+ * nothing stays allocated.  Host-pool contents are left uninitialised. */
+hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out);
+
+/* Free everything the pool owns.  Synchronises the device first. */
+hs_status hs_pool_destroy(hs_pool* pool);
+
+/* Raw pointers for inspection and bulk set-up (e.g. filling host_pool).  The
+ * pool keeps ownership; pointers stay valid until hs_pool_destroy. */
+hs_status hs_pool_get_views(const hs_pool* pool, hs_pool_views* out);
+
+/* Reset the LRU metadata of every unit (slots empty, stamp -1, identity
+ * order), the step counter and the error word.  Async on `stream`. */
+hs_status hs_pool_reset(hs_pool* pool, void* stream);
+
+/* Set a request's current context length and its first row in the host pool.
+ * Async on `stream`, graph-capturable.  HS_ERR_INVALID if req is out of range,
+ * ctx_len > max_pages * P or host_off + ctx_len > host_tokens. */
+hs_status hs_set_request(hs_pool* pool, int32_t req, int32_t ctx_len,
+                         int64_t host_off, void* stream);
+
+/* page_table[req][page] = block (block -1 marks the page host only).  Async on
+ * `stream`, graph-capturable.  HS_ERR_INVALID if block is a hot-buffer block
+ * or outside the pool. */
+hs_status hs_map_page(hs_pool* pool, int32_t req, int32_t page, int32_t block,
+                      void* stream);
+
+/* Make a page resident: copy its rows of every layer from the host pool into
+ * `block`, then map it.  Async on `stream` (set-up path). */
+hs_status hs_load_page(hs_pool* pool, int32_t req, int32_t page, int32_t block,
+                       void* stream);
+
+/* RESOLVE (one launch for layers layer_begin .. layer_begin+num_layers-1,
+ * one CTA per (request, layer) unit).  For every unit and j < K:
+ *   p = topk_idx[i][r][j]; -1 is padding (row id -1);
+ *   a resident page gives block*P + p%P, LRU untouched;
+ *   a hot hit gives the slot's row and stamps it with *d_step;
+ *   each miss (in j order) takes the next slot with stamp < *d_step in
+ *   (stamp, slot) order, gets stamp *d_step and receives a copy of host row
+ *   host_off[r] + p of layer l, loaded by the kernel from mapped pinned memory.
+ * Hits are refreshed before misses are served, so a slot used in this step is
+ * never a victim.
+ *   topk_idx     device int32 [num_layers][R][K]          (caller-owned)
+ *   d_step       device int32 scalar (e.g. views.step), read by the kernel, so
+ *                a captured CUDA graph replays with the current step
+ *   out_row_ids  device int32 [num_layers][R][K]          (caller-owned)
+ *   miss_count   device int32 [num_layers][R] or NULL: misses served
+ *   miss_log     device int32 [num_layers][R][K][3] or NULL: (j, position,
+ *                slot) of each served miss in j order; later entries undefined
+ * Async on `stream`; no host synchronisation, no allocation; graph-capturable.
+ * Device-side errors: bits RANGE, DUPLICATE, CAPACITY, BLOCK. */
+hs_status hs_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
+                     const int32_t* topk_idx, const int32_t* d_step,
+                     int32_t* out_row_ids, int32_t* miss_count,
+                     int32_t* miss_log, void* stream);
+
+/* Gather rows of one layer by row id ("one stride"): out_rows[i] =
+ * kv_pool[layer][row_ids[i]] (row_elems bf16 each); row id -1 gives a zero
+ * row.  row_ids: device int32 [n_rows]; out_rows: device bf16
+ * [n_rows][row_elems] (caller-owned).  Async, graph-capturable.  A row id
+ * outside the layer writes a zero row and sets error bit BLOCK. */
+hs_status hs_gather(hs_pool* pool, int32_t layer, const int32_t* row_ids,
+                    int64_t n_rows, void* out_rows, void* stream);
+
+/* Sparse MLA decode attention of one layer over exactly the K rows each
+ * request resolved (absorbed MLA, page "GLM 5.3 Optimizations, Part 1"
+ * section "How it works": the sparse MLA kernel reads hot and resident rows
+ * alike by row id):
+ *   s[h][j]  = scale * sum_{d<row_elems} q[r][h][d] * kv(row_ids[r][j])[d]
+ *   out[r][h][e] = sum_j softmax_j(s[h][.]) * kv(row_ids[r][j])[e],  e < v_dim
+ * over the j with row_ids >= 0 (v = the first v_dim = 512 columns of each
+ * row).  bf16 inputs, fp32 accumulation on the tensor cores, bf16 output.
+ *   q        device bf16 [R][num_heads][row_elems]   (num_heads <= 128)
+ *   row_ids  device int32 [R][K] (e.g. hs_resolve's output for this layer)
+ *   out      device bf16 [R][num_heads][v_dim]
+ *   lse      device float [R][num_heads] or NULL: natural-log sum of exp of
+ *            the scores (-inf when a request has no valid row; out is then 0)
+ * Async, graph-capturable; uses the pool's workspace (calls on one pool must
+ * not overlap on the GPU). */
+hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, const void* q,
+                               const int32_t* row_ids, int32_t num_heads,
+                               int32_t v_dim, float scale, void* out,
+                               float* lse, void* stream);
+
+/* Prefix offload: copy page `page` of request `req` (all layers, from the
+ * block the page table maps it to) into its rows of the host pool.  The copy
+ * is one kernel launch on `side_stream`, ordered after the work queued so far
+ * on `main_stream`; `done_event` (caller-owned cudaEvent_t) is recorded on
+ * `side_stream` after it.  The page stays mapped and readable on the GPU.
+ * HS_ERR_INVALID if the page is not resident or lies beyond the host rows of
+ * the request. */
+hs_status hs_offload_prefix(hs_pool* pool, int32_t req, int32_t page,
+                            void* main_stream, void* side_stream,
+                            void* done_event);
+
+/* Make `main_stream` wait for `done_event`, then mark the page host only
+ * (page_table = -1).  The freed block may be mapped again afterwards. */
+hs_status hs_commit_offload(hs_pool* pool, int32_t req, int32_t page,
+                            void* main_stream, void* done_event);
+
+/* *d_step += 1 on `stream` (graph-capturable). */
+hs_status hs_step_advance(int32_t* d_step, void* stream);
+
+/* Synchronise the device, read and clear the device error word into
+ * *code_out.  Returns HS_OK if it was zero, HS_ERR_DEVICE otherwise. */
+hs_status hs_check_errors(hs_pool* pool, int32_t* code_out);
+
+/* Static string naming a status. */
+const char* hs_status_string(hs_status status);
+
+/* Library version string. */
+const char* hs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HS_H */

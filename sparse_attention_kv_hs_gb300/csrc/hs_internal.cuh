@@ -1,0 +1,56 @@
+// Internal definitions shared by the libhs translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "hs.h"
+
+struct hs_pool {
+  hs_pool_desc d;
+  int device;
+  int num_sms;
+  int64_t blocks_per_layer;
+  int64_t hot_blocks;  // R * B / P, per layer
+
+  void* kv_pool;  // device bf16 [L][blocks_per_layer][P][row_elems]
+  size_t kv_bytes;
+  void* host_pool;      // pinned host
+  void* host_pool_dev;  // device alias
+  size_t host_bytes;
+
+  int32_t* page_table;  // [R][max_pages]
+  int32_t* ctx_len;     // [R]
+  int64_t* host_off;    // [R]
+  int32_t* hot_block;   // [R][B/P]
+  int32_t* slot_pos;    // [L][R][B]
+  int32_t* slot_stamp;  // [L][R][B]
+  int32_t* lru_order;   // [L][R][B]
+  int32_t* step;        // scalar
+  int32_t* error_word;  // scalar
+
+  // sparse MLA decode workspace (split-K partials)
+  float* attn_o;    // [R][max_splits][128][512]
+  float* attn_ml;   // [R][max_splits][128] lse
+  int attn_max_splits;
+
+  cudaEvent_t order_event;  // orders offload copies after main-stream work
+  int64_t* host_off_mirror; // host copy of host_off (set-up calls only)
+};
+
+#define HS_CUDA_TRY(expr)                       \
+  do {                                          \
+    cudaError_t e_ = (expr);                    \
+    if (e_ != cudaSuccess) return HS_ERR_CUDA;  \
+  } while (0)
+
+static inline cudaStream_t hs_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Launch wrappers implemented per translation unit.
+hs_status hs_launch_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
+                            const int32_t* topk, const int32_t* d_step, int32_t* out_rows,
+                            int32_t* miss_count, int32_t* miss_log, cudaStream_t stream);
+hs_status hs_attn_workspace_init(hs_pool* pool);
+// Shared memory the RESOLVE kernel needs for these sizes; sets the kernel's
+// dynamic shared-memory limit (call once per pool, outside stream capture).
+hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes);
