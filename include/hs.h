@@ -193,8 +193,9 @@ hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, const void* q,
  * is one kernel launch on `side_stream`, ordered after the work queued so far
  * on `main_stream`; `done_event` (caller-owned cudaEvent_t) is recorded on
  * `side_stream` after it.  The page stays mapped and readable on the GPU.
- * HS_ERR_INVALID if the page is not resident or lies beyond the host rows of
- * the request. */
+ * HS_ERR_INVALID for out-of-range arguments; if the page is not mapped to a
+ * resident block when the copy runs, nothing is copied and the kernel sets
+ * device error bit BLOCK. */
 hs_status hs_offload_prefix(hs_pool* pool, int32_t req, int32_t page,
                             void* main_stream, void* side_stream,
                             void* done_event);
@@ -203,6 +204,13 @@ hs_status hs_offload_prefix(hs_pool* pool, int32_t req, int32_t page,
  * (page_table = -1).  The freed block may be mapped again afterwards. */
 hs_status hs_commit_offload(hs_pool* pool, int32_t req, int32_t page,
                             void* main_stream, void* done_event);
+
+/* Copy `bytes` (a multiple of 16) from mapped pinned host memory (its device
+ * alias, e.g. views.host_pool_device) to device memory `dst` with SM loads --
+ * the access path RESOLVE uses for miss rows -- so its bandwidth is the
+ * ceiling of the in-kernel miss copy.  Async on `stream`.  HS_ERR_INVALID for
+ * null or misaligned pointers. */
+hs_status hs_host_read(const void* host_device_ptr, int64_t bytes, void* dst, void* stream);
 
 /* *d_step += 1 on `stream` (graph-capturable). */
 hs_status hs_step_advance(int32_t* d_step, void* stream);

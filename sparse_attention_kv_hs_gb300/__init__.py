@@ -35,7 +35,7 @@ EXPORTED = (
     "hs_pool_create", "hs_pool_destroy", "hs_pool_get_views", "hs_pool_reset",
     "hs_set_request", "hs_map_page", "hs_load_page", "hs_resolve", "hs_gather",
     "hs_sparse_mla_decode", "hs_offload_prefix", "hs_commit_offload",
-    "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version",
+    "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
 )
 
 
@@ -97,6 +97,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_commit_offload": [p, i32, i32, p, p],
         "hs_step_advance": [p, p],
         "hs_check_errors": [p, ctypes.POINTER(i32)],
+        "hs_host_read": [p, i64, p, p],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -229,6 +230,11 @@ def hs_check_errors(pool: int) -> int:
     if st not in (HS_OK, HS_ERR_DEVICE):
         raise HsError(st, "hs_check_errors")
     return code.value
+
+
+def hs_host_read(host_device_ptr: int, nbytes: int, dst, stream=None) -> None:
+    _check(load().hs_host_read(host_device_ptr, nbytes, _addr(dst), _stream(stream)),
+           "hs_host_read")
 
 
 def hs_version() -> str:

@@ -1,17 +1,640 @@
-// Sparse MLA decode attention (work in progress: entry point only).
+// Sparse MLA decode attention over the K rows RESOLVE handed out, on the
+// sm_100-family tensor cores (tcgen05, fp32 accumulators in tensor memory).
+//
+// What it computes (absorbed MLA decode; the sparse MLA kernel of page "GLM
+// 5.3 Optimizations, Part 1: Hybrid HiSparse Offloading in vLLM", section "How
+// it works", reads hot-buffer and resident rows alike by row id): for each
+// request r and head h < 128,
+//   s_j = scale * q[h] . kv(row_ids[r][j])            (576-wide rows)
+//   out[h] = sum_j softmax(s)_j * kv(row_ids[r][j])[0:512]
+// over the j with a valid row id.
+//
+// Work split.  The fp32 output accumulator O (128 heads x 512) fills a whole
+// SM's tensor memory, so each (request, split-of-K) is handled by a CTA pair
+// (a cluster of 2):
+//   CTA 0 ("score"): Q lives in tensor memory (the A operand), 64-row KV tiles
+//     are staged in shared memory by cp.async, S = Q K^T (M=128, N=64, K=576)
+//     goes to a double-buffered TMEM accumulator, 4 warps run the online
+//     softmax (one thread per head) and write P as two bf16 parts (hi + lo,
+//     so P carries ~16 bits: bf16 P alone would cost ~1e-3 relative error)
+//     which one bulk copy sends into CTA 1's shared memory.
+//   CTA 1 ("value"): stages the V part (first 512 columns) of the same rows
+//     and accumulates O += P_hi V + P_lo V (M=128, N=256 x 2).  Its 4 epilogue
+//     warps rescale O when the running max moved (lazily: only when it grew by
+//     more than 2^8, so the rescale is rare and off the common path) and write
+//     the normalised output.
+// Q reaches CTA 0 by one bulk copy (then TMEM), each split's row ids are
+// staged in shared memory once, and every hand-off is an mbarrier.
+// With several splits per request, each pair writes a normalised fp32 partial
+// and its log-sum-exp; a small merge kernel combines them.
+//
+// Every wait is bounded: a wait that times out sets HS_DEV_ERR_WAIT in the
+// pool's error word and the CTA winds down (no further MMAs), frees its tensor
+// memory and exits.
+#include <cuda_bf16.h>
+#include <math.h>
+
 #include "hs_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace {
+
+using namespace hs_ptx;
+
+constexpr int kHeads = 128;        // MMA M (heads, zero-padded)
+constexpr int kD = 576;            // row width (latent 512 + rope 64)
+constexpr int kDV = 512;           // value width
+constexpr int kTile = 64;          // KV rows per tile
+constexpr int kStages = 2;         // KV tile ring depth
+constexpr int kThreads = 256;
+constexpr int kLoadWarps = 3;      // warps 1..3
+constexpr int kLoaders = kLoadWarps * 32;
+constexpr int kCoreD = kD / 8;     // 72 core-matrix columns per row group (score tile)
+constexpr int kCoreV = kDV / 8;    // 64 (value tile)
+
+constexpr uint32_t kStageBytes = kTile * kD * 2;          // 73728
+constexpr uint32_t kPBytes = kHeads * kTile * 2;          // 16384 per part
+constexpr uint32_t kPMetaBytes = 528;                     // alpha[128] floats + 4 flag words
+constexpr uint32_t kPCopyBytes = 2 * kPBytes + kPMetaBytes;   // 33296 (multiple of 16)
+constexpr uint32_t kPBufBytes = 2 * kPBytes + 1024;       // 33792
+
+// Shared-memory layout, identical offsets in both CTAs of a pair (the bulk
+// copy and remote barrier operations address the peer by offset).
+constexpr int kMaxSplitRows = 2048;  // row ids of one split, staged in shared memory
+constexpr uint32_t OFF_STAGE = 0;    // CTA 0 first holds Q here (<= 147456 B)
+constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // 147456
+constexpr uint32_t OFF_ML = OFF_P + 2 * kPBufBytes;            // 215040: m[128], l[128]
+constexpr uint32_t OFF_RID = OFF_ML + 1024;                    // 216064: int32 [2048]
+constexpr uint32_t OFF_BAR = OFF_RID + 4 * kMaxSplitRows;      // 224256
+constexpr uint32_t OFF_MISC = OFF_BAR + 256;
+constexpr uint32_t kSmemBytes = OFF_MISC + 64;                 // 224576
+static_assert(kHeads * kD * 2 <= kStages * kStageBytes, "Q must fit the stage region");
+
+// barrier indices (8 bytes each at OFF_BAR)
+enum {
+  B_KV_FULL = 0,     // [2] loaders -> MMA (both CTAs: K tile / V tile)
+  B_KV_EMPTY = 2,    // [2] MMA commit -> loaders
+  B_S_FULL = 4,      // [2] score MMA commit -> softmax
+  B_S_EMPTY = 6,     // [2] softmax -> score MMA
+  B_P_EMPTY = 8,     // [2] (CTA 0) value MMA commit (multicast) -> softmax
+  B_Q_SMEM = 10,     // (CTA 0) bulk copy of Q landed in shared memory
+  B_Q_READY = 11,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loaders
+  B_P_FULL = 12,     // [2] (CTA 1) bulk copy complete_tx -> value MMA
+  B_RID = 14,        // loaders staged this split's row ids
+  B_CORR_REQ = 15,   // (CTA 1) value MMA -> rescale warps
+  B_CORR_DONE = 16,  // (CTA 1) rescale warps -> value MMA
+  B_MMA_IDLE = 17,   // (CTA 1) commit: earlier P.V MMAs finished
+  B_ML_FULL = 18,    // (CTA 1) softmax's final m, l -> epilogue
+  B_FINAL = 19,      // MMA issuer's last commit
+  B_P_READY = 20,    // [2] (CTA 0) softmax threads wrote P -> bulk-copy issuer
+  B_COUNT = 22
+};
+static_assert(B_COUNT * 8 <= 256, "barrier area");
+
+// TMEM columns
+constexpr uint32_t TM_Q = 0;     // CTA 0: Q, 288 columns (bf16 pairs)
+constexpr uint32_t TM_S = 288;   // CTA 0: S, 2 x 64 columns
+constexpr uint32_t TM_O = 0;     // CTA 1: O, 512 columns
+
+constexpr uint32_t kIdescS = idesc_bf16(128, kTile, false, false);  // K-major A (TMEM), K-major B
+constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // K-major A, MN-major B
+
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before giving up
+
+struct AttnArgs {
+  const uint16_t* q;        // [R][H][576]
+  const int32_t* row_ids;   // [R][K]
+  const uint16_t* kv;       // layer base [rows][576]
+  uint16_t* out;            // [R][H][512] bf16 (splits == 1)
+  float* lse;               // [R][H] or null (splits == 1)
+  float* ws_o;              // [R][splits][128][512] (splits > 1)
+  float* ws_lse;            // [R][splits][128]
+  int32_t* error_word;
+  int64_t rows_in_layer;
+  int32_t K, H, splits, rows_per_split;
+  float scale_log2;         // scale * log2(e)
+};
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on a local mbarrier; on timeout (or if the CTA is already
+// aborting) returns false and raises the abort flag.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort,
+                                         int32_t* error_word, bool cluster_scope = false) {
+  if (*abort) return false;
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    const bool ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    if (ok) return true;
+    if ((i & 63) == 63) {
+      if (*abort) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitNs) {
+        *abort = 1;
+        atomicOr(error_word, HS_DEV_ERR_WAIT);
+        return false;
+      }
+    }
+  }
+}
+
+// Same, for roles run by whole warps: every lane gets the same answer, so
+// warp-collective tcgen05 instructions after it are executed uniformly.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              int32_t* error_word, bool cluster_scope = false) {
+  const bool ok = wait_bar(bar, parity, abort, error_word, cluster_scope);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// 2^x (hardware approximation, relative error ~2^-22; 2^-inf = 0)
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Stage one 64-row tile (row ids already validated, -1 = zero row), `ncore`
+// 16-byte core columns per row, into the no-swizzle K-major core-matrix
+// layout (row group rb, core column cb at (rb*ncore + cb)*128, row%8 at +16).
+// Each warp instruction moves 8 rows x 4 core columns = 4 whole core matrices.
+__device__ __forceinline__ void load_tile(uint32_t stage, const uint16_t* kv,
+                                          const int32_t* s_rid_tile, int ncore, int lwarp,
+                                          int lane) {
+  const int quads = ncore / 4;
+  const int sub = lane & 7, cq = lane >> 3;
+  int item = 0;  // work items (row group, quad of core columns) dealt round-robin to the warps
+#pragma unroll
+  for (int rb = 0; rb < 8; ++rb) {
+    const int32_t r = s_rid_tile[rb * 8 + sub];
+    const uint16_t* row = r >= 0 ? kv + (int64_t)r * kD : kv;
+    const uint32_t src_bytes = r >= 0 ? 16u : 0u;
+    const uint32_t dst_row = stage + (uint32_t)(rb * ncore * 128 + sub * 16);
+    int q = (lwarp - item % kLoadWarps + kLoadWarps) % kLoadWarps;
+    for (; q < quads; q += kLoadWarps) {
+      const int cb = q * 4 + cq;
+      cp_async_16(dst_row + (uint32_t)(cb * 128), r >= 0 ? row + cb * 8 : kv, src_bytes);
+    }
+    item += quads;
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mla_decode_kernel(const AttnArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + OFF_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  volatile int* corr_tile = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);
+  volatile int* corr_exit = reinterpret_cast<volatile int*>(smem + OFF_MISC + 12);
+  int32_t* s_rid = reinterpret_cast<int32_t*>(smem + OFF_RID);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int split = blockIdx.x >> 1;
+  const int r = blockIdx.y;
+  const int j_begin = split * a.rows_per_split;
+  int j_end = j_begin + a.rows_per_split;
+  if (j_end > a.K) j_end = a.K;
+  const int n_tiles = j_end > j_begin ? (j_end - j_begin + kTile - 1) / kTile : 0;
+
+  // ---- set-up: barriers, tensor memory ---------------------------------
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_KV_FULL + i), kLoaders);
+      mbar_init(bar(B_KV_EMPTY + i), 1);
+      mbar_init(bar(B_S_FULL + i), 1);
+      mbar_init(bar(B_S_EMPTY + i), 128);
+      mbar_init(bar(B_P_EMPTY + i), 1);
+      mbar_init(bar(B_P_FULL + i), 1);
+      mbar_init(bar(B_P_READY + i), 128);
+    }
+    mbar_init(bar(B_Q_SMEM), 1);
+    mbar_init(bar(B_Q_READY), 128);
+    mbar_init(bar(B_RID), kLoaders);
+    mbar_init(bar(B_CORR_REQ), 1);
+    mbar_init(bar(B_CORR_DONE), 128);
+    mbar_init(bar(B_MMA_IDLE), 1);
+    mbar_init(bar(B_ML_FULL), 128);
+    mbar_init(bar(B_FINAL), 1);
+    *abort_flag = 0;
+    *corr_tile = 0;
+    *corr_exit = 0;
+    fence_mbar_init_cluster();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // the peer's barriers exist before any remote operation
+  const uint32_t tm = *tmem_holder;
+  int err = 0;
+
+  if (warp >= 1 && warp <= kLoadWarps) {
+    // ================= loaders (both CTAs) =================
+    const int lt = tid - 32, lwarp = warp - 1;
+    if (rank == 0 && lt == 0) {  // Q[r] (H x 576 bf16, contiguous) -> shared memory
+      const uint32_t qbytes = (uint32_t)a.H * kD * 2;
+      mbar_arrive_expect_tx(bar(B_Q_SMEM), qbytes);
+      bulk_copy_g2s(sbase + OFF_STAGE, a.q + (int64_t)r * a.H * kD, qbytes, bar(B_Q_SMEM));
+    }
+    // this split's row ids -> shared memory, validated once (-1 = no row)
+    const int32_t* g_rows = a.row_ids + (int64_t)r * a.K;
+    for (int i = lt; i < n_tiles * kTile; i += kLoaders) {
+      const int j = j_begin + i;
+      int32_t v = j < j_end ? __ldg(g_rows + j) : -1;
+      if (v < -1 || v >= a.rows_in_layer) {
+        err |= HS_DEV_ERR_BLOCK;
+        v = -1;
+      }
+      s_rid[i] = v;
+    }
+    asm volatile("bar.sync 2, 96;" ::: "memory");  // the 3 loader warps, unconditionally
+    mbar_arrive(bar(B_RID));
+    const int ncore = rank == 0 ? kCoreD : kCoreV;
+    // CTA 0: Q occupies the stage region until it has moved to TMEM
+    bool ok = rank == 0 ? wait_bar(bar(B_Q_READY), 0, abort_flag, a.error_word) : true;
+    for (int t = 0; ok && t < n_tiles; ++t) {
+      const int s = t % kStages;
+      const uint32_t ph = (uint32_t)(t / kStages) & 1u;
+      if (!wait_bar(bar(B_KV_EMPTY + s), ph ^ 1u, abort_flag, a.error_word)) break;
+      load_tile(sbase + OFF_STAGE + s * kStageBytes, a.kv, s_rid + t * kTile, ncore, lwarp, lane);
+      cp_async_arrive(bar(B_KV_FULL + s));
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == 0) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      if (rank == 0) {
+        if (wait_bar(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
+          tc_fence_after();
+          for (int t = 0; t < n_tiles; ++t) {
+            const int s = t % kStages, b = t & 1;
+            const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t >> 1) & 1u;
+            if (!wait_bar(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
+            if (!wait_bar(bar(B_S_EMPTY + b), pb ^ 1u, abort_flag, a.error_word)) break;
+            tc_fence_after();
+            const uint32_t kst = sbase + OFF_STAGE + s * kStageBytes;
+#pragma unroll 4
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ts(tm + TM_S + b * kTile, tm + TM_Q + kk * 8,
+                     smem_desc(kst + kk * 256, 128, kCoreD * 128), kIdescS, kk > 0);
+            mma_commit(bar(B_KV_EMPTY + s));
+            mma_commit(bar(B_S_FULL + b));
+          }
+        }
+      } else {
+        uint32_t corr = 0;
+        for (int t = 0; t < n_tiles; ++t) {
+          const int s = t % kStages, b = t & 1;
+          const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t >> 1) & 1u;
+          mbar_arrive_expect_tx(bar(B_P_FULL + b), kPCopyBytes);
+          if (!wait_bar(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
+          if (!wait_bar(bar(B_P_FULL + b), pb, abort_flag, a.error_word, true)) break;
+          const uint32_t pbuf = sbase + OFF_P + b * kPBufBytes;
+          const uint32_t* flags =
+              reinterpret_cast<const uint32_t*>(smem + OFF_P + b * kPBufBytes + 2 * kPBytes + 512);
+          if (t > 0 && (flags[0] | flags[1] | flags[2] | flags[3])) {
+            // the running max moved for some head: rescale O before adding tile t
+            mma_commit(bar(B_MMA_IDLE));
+            if (!wait_bar(bar(B_MMA_IDLE), corr & 1u, abort_flag, a.error_word)) break;
+            *corr_tile = t;
+            mbar_arrive(bar(B_CORR_REQ));
+            if (!wait_bar(bar(B_CORR_DONE), corr & 1u, abort_flag, a.error_word)) break;
+            ++corr;
+          }
+          tc_fence_after();
+          const uint32_t vst = sbase + OFF_STAGE + s * kStageBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+              const uint64_t adesc = smem_desc(pbuf + part * kPBytes + kk * 256, 128, 1024);
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint64_t bdesc =
+                    smem_desc(vst + kk * 2 * (kCoreV * 128) + half * 4096, kCoreV * 128, 128);
+                mma_ss(tm + TM_O + half * 256, adesc, bdesc, kIdescPV,
+                       (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
+              }
+            }
+          }
+          mma_commit(bar(B_KV_EMPTY + s));
+          mma_commit_multicast(bar(B_P_EMPTY + b), (uint16_t)0x1);  // P buffer b free (CTA 0)
+        }
+        *corr_exit = 1;
+        mbar_arrive(bar(B_CORR_REQ));  // releases the rescale warps
+      }
+      mma_commit(bar(B_FINAL));
+      wait_bar(bar(B_FINAL), 0, abort_flag, a.error_word);
+    }
+    __syncwarp();
+  } else if (rank == 0) {
+    // ================= softmax (CTA 0, warps 4..7, one thread per head) =================
+    const int h = tid - 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = wait_bar_warp(bar(B_Q_SMEM), 0, abort_flag, a.error_word);
+    if (ok) {  // Q[h] -> TMEM columns TM_Q .. TM_Q+287 (bf16 pairs), zero for padded heads
+      const uint4* qs = reinterpret_cast<const uint4*>(smem + OFF_STAGE) + h * (kD / 8);
+      for (int c0 = 0; c0 < kD / 2; c0 += 16) {
+        uint32_t v[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (h < a.H) x = qs[c0 / 4 + i];
+          v[4 * i + 0] = x.x;
+          v[4 * i + 1] = x.y;
+          v[4 * i + 2] = x.z;
+          v[4 * i + 3] = x.w;
+        }
+        tmem_st16(tm + lane_off + TM_Q + c0, v);
+      }
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    mbar_arrive(bar(B_Q_READY));
+    ok = ok && wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word);
+    const uint32_t peer_p = mapa(sbase + OFF_P, 1);
+    const uint32_t peer_pfull = mapa(bar(B_P_FULL), 1);
+    float m_used = -INFINITY, l_sum = 0.f;
+    for (int t = 0; ok && t < n_tiles; ++t) {
+      const int b = t & 1;
+      const uint32_t pb = (uint32_t)(t >> 1) & 1u;
+      const uint64_t valid =
+          (uint64_t)__ballot_sync(0xffffffffu, s_rid[t * kTile + lane] >= 0) |
+          ((uint64_t)__ballot_sync(0xffffffffu, s_rid[t * kTile + lane + 32] >= 0) << 32);
+      if (!wait_bar_warp(bar(B_S_FULL + b), pb, abort_flag, a.error_word)) break;
+      tc_fence_after();
+      float x[kTile];
+#pragma unroll
+      for (int c = 0; c < kTile; c += 16) {
+        uint32_t u[16];
+        tmem_ld16(tm + lane_off + TM_S + b * kTile + c, u);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(u[i]);
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_S_EMPTY + b));
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kTile; ++i) {
+        x[i] = ((valid >> i) & 1) ? x[i] * a.scale_log2 : -INFINITY;
+        tmax = fmaxf(tmax, x[i]);
+      }
+      // lazy rescale: move the reference max only when it grew by > 2^8
+      const bool rescale = tmax > m_used + 8.f;
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = fast_exp2(m_used - tmax);  // 0 when m_used is -inf
+        l_sum *= alpha;
+        m_used = tmax;
+      }
+      // P buffer b is free once the value CTA finished tile t-2
+      if (!wait_bar_warp(bar(B_P_EMPTY + b), pb ^ 1u, abort_flag, a.error_word)) break;
+      unsigned char* pbuf = smem + OFF_P + b * kPBufBytes;
+#pragma unroll
+      for (int kb = 0; kb < kTile / 8; ++kb) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = x[kb * 8 + 2 * i], x1 = x[kb * 8 + 2 * i + 1];
+          const float p0 = x0 == -INFINITY ? 0.f : fast_exp2(x0 - m_used);
+          const float p1 = x1 == -INFINITY ? 0.f : fast_exp2(x1 - m_used);
+          l_sum += p0 + p1;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          const float2 hf = __bfloat1622float2(h2);
+          hi[i] = *reinterpret_cast<const uint32_t*>(&h2);
+          lo[i] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
+        }
+        // P [128 heads x 64 rows], K-major core matrices (head group, row group)
+        const uint32_t off = (uint32_t)(((h >> 3) * (kTile / 8) + kb) * 128 + (h & 7) * 16);
+        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(pbuf + kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      float* meta = reinterpret_cast<float*>(pbuf + 2 * kPBytes);
+      meta[h] = alpha;
+      const uint32_t any = __ballot_sync(0xffffffffu, rescale && t > 0);
+      if (lane == 0) reinterpret_cast<uint32_t*>(meta + 128)[warp & 3] = any;
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk copy
+      mbar_arrive(bar(B_P_READY + b));
+      if (h == 0) {
+        if (!wait_bar(bar(B_P_READY + b), pb, abort_flag, a.error_word)) break;
+        bulk_copy_s2cluster(peer_p + b * kPBufBytes, sbase + OFF_P + b * kPBufBytes, kPCopyBytes,
+                            peer_pfull + 8u * b);
+      }
+    }
+    // final m, l for this head -> value CTA
+    st_cluster_f32(mapa(sbase + OFF_ML + 4 * h, 1), m_used);
+    st_cluster_f32(mapa(sbase + OFF_ML + 512 + 4 * h, 1), l_sum);
+    mbar_arrive_remote(mapa(bar(B_ML_FULL), 1));
+    // wait until the value CTA released the last P buffers (its commits landed)
+    for (int t = n_tiles - 2; t < n_tiles; ++t) {
+      if (t < 0) continue;
+      wait_bar(bar(B_P_EMPTY + (t & 1)), (uint32_t)(t >> 1) & 1u, abort_flag, a.error_word);
+    }
+  } else {
+    // ================= rescale + epilogue (CTA 1, warps 4..7) =================
+    const int h = tid - 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    for (uint32_t k = 0;; ++k) {  // rare: only tiles where some head's max moved
+      if (!wait_bar_warp(bar(B_CORR_REQ), k & 1u, abort_flag, a.error_word)) break;
+      if (*corr_exit) break;
+      tc_fence_after();
+      const int t = *corr_tile;
+      const float alpha =
+          reinterpret_cast<const float*>(smem + OFF_P + (t & 1) * kPBufBytes + 2 * kPBytes)[h];
+      if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        for (int c = 0; c < kDV; c += 16) {
+          uint32_t u[16];
+          tmem_ld16(tm + lane_off + TM_O + c, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st16(tm + lane_off + TM_O + c, u);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar(B_CORR_DONE));
+    }
+    // epilogue: O / l
+    bool ok = wait_bar_warp(bar(B_FINAL), 0, abort_flag, a.error_word) && n_tiles > 0;
+    const bool have_ml = wait_bar_warp(bar(B_ML_FULL), 0, abort_flag, a.error_word, true);
+    ok = ok && have_ml;  // warp-uniform: gates the warp-collective TMEM loads below
+    tc_fence_after();
+    const float m = have_ml ? reinterpret_cast<const float*>(smem + OFF_ML)[h] : -INFINITY;
+    const float l = have_ml ? reinterpret_cast<const float*>(smem + OFF_ML + 512)[h] : 0.f;
+    const bool has_rows = ok && l > 0.f;  // per head (lane)
+    const float inv_l = has_rows ? 1.f / l : 0.f;
+    const float lse = has_rows ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    const bool write = h < a.H;
+    if (a.splits == 1) {
+      uint16_t* orow = a.out + ((int64_t)r * a.H + (write ? h : 0)) * kDV;
+      for (int c = 0; c < kDV; c += 16) {
+        uint32_t u[16];
+        if (ok) {
+          tmem_ld16(tm + lane_off + TM_O + c, u);
+          tmem_ld_wait();
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pk[i] = has_rows ? pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l,
+                                         __uint_as_float(u[2 * i + 1]) * inv_l)
+                           : 0u;
+        if (write) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      if (write && a.lse) a.lse[(int64_t)r * a.H + h] = lse;
+    } else {
+      float* orow = a.ws_o + (((int64_t)r * a.splits + split) * kHeads + h) * kDV;
+      for (int c = 0; c < kDV; c += 16) {
+        uint32_t u[16];
+        if (ok) {
+          tmem_ld16(tm + lane_off + TM_O + c, u);
+          tmem_ld_wait();
+        }
+        float4* dst = reinterpret_cast<float4*>(orow + c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = has_rows ? make_float4(__uint_as_float(u[4 * i]) * inv_l,
+                                          __uint_as_float(u[4 * i + 1]) * inv_l,
+                                          __uint_as_float(u[4 * i + 2]) * inv_l,
+                                          __uint_as_float(u[4 * i + 3]) * inv_l)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      a.ws_lse[((int64_t)r * a.splits + split) * kHeads + h] = lse;
+    }
+  }
+
+  if (err) atomicOr(a.error_word, err);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, 512);
+  cluster_sync();
+}
+
+// Combine per-split normalised partials: o = sum_c w_c o_c / sum_c w_c with
+// w_c = exp(lse_c - max lse).  One CTA per (request, head), 128 threads x 4.
+__global__ void __launch_bounds__(128) merge_splits_kernel(const float* __restrict__ ws_o,
+                                                           const float* __restrict__ ws_lse,
+                                                           int splits, int H,
+                                                           uint16_t* __restrict__ out,
+                                                           float* __restrict__ lse_out) {
+  const int r = blockIdx.y, h = blockIdx.x;
+  float mx = -INFINITY;
+  for (int c = 0; c < splits; ++c) mx = fmaxf(mx, ws_lse[((int64_t)r * splits + c) * kHeads + h]);
+  float wsum = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int e0 = threadIdx.x * 4;
+  for (int c = 0; c < splits; ++c) {
+    const float lc = ws_lse[((int64_t)r * splits + c) * kHeads + h];
+    const float w = lc == -INFINITY ? 0.f : expf(lc - mx);
+    wsum += w;
+    const float4 o = *reinterpret_cast<const float4*>(
+        ws_o + (((int64_t)r * splits + c) * kHeads + h) * kDV + e0);
+    acc[0] += w * o.x;
+    acc[1] += w * o.y;
+    acc[2] += w * o.z;
+    acc[3] += w * o.w;
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint2 pk;
+  pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  *reinterpret_cast<uint2*>(out + ((int64_t)r * H + h) * kDV + e0) = pk;
+  if (lse_out && threadIdx.x == 0)
+    lse_out[(int64_t)r * H + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
+}
+
+// Splits of K per request: enough CTA pairs to cover the SMs once.
+// At most kMaxSplitRows rows per split (their ids are staged in shared memory).
+int choose_splits(int num_sms, int R, int K) {
+  const int tiles = (K + kTile - 1) / kTile;
+  int s = num_sms / (2 * R);
+  if (s < 1) s = 1;
+  if (s > tiles) s = tiles;
+  const int min_s = (tiles * kTile + kMaxSplitRows - 1) / kMaxSplitRows;
+  if (s < min_s) s = min_s;
+  return s;
+}
+
+}  // namespace
 
 hs_status hs_attn_workspace_init(hs_pool* p) {
   p->attn_o = nullptr;
   p->attn_ml = nullptr;
   p->attn_max_splits = 0;
+  if (p->d.row_elems != kD) return HS_OK;  // attention needs 576-wide rows; decode call rejects
+  HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kSmemBytes));
+  const int splits = choose_splits(p->num_sms, p->d.num_requests, p->d.top_k);
+  p->attn_max_splits = splits;
+  if (splits > 1) {
+    const size_t n = (size_t)p->d.num_requests * splits * kHeads;
+    if (cudaMalloc(&p->attn_o, n * kDV * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&p->attn_ml, n * sizeof(float)) != cudaSuccess) {
+      cudaGetLastError();
+      return HS_ERR_OOM;
+    }
+  }
   return HS_OK;
 }
 
-extern "C" hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, const void* q,
+extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void* q,
                                           const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
                                           float scale, void* out, float* lse, void* stream) {
-  (void)pool; (void)layer; (void)q; (void)row_ids; (void)num_heads; (void)v_dim; (void)scale;
-  (void)out; (void)lse; (void)stream;
-  return HS_ERR_INVALID;
+  if (!p || !q || !row_ids || !out) return HS_ERR_INVALID;
+  if (layer < 0 || layer >= p->d.num_layers || num_heads <= 0 || num_heads > kHeads ||
+      v_dim != kDV || p->d.row_elems != kD || !(scale > 0.f) || p->attn_max_splits < 1)
+    return HS_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return HS_ERR_INVALID;
+  const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
+  AttnArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.row_ids = row_ids;
+  a.kv = static_cast<const uint16_t*>(p->kv_pool) + (int64_t)layer * rows_in_layer * kD;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.ws_o = p->attn_o;
+  a.ws_lse = p->attn_ml;
+  a.error_word = p->error_word;
+  a.rows_in_layer = rows_in_layer;
+  a.K = p->d.top_k;
+  a.H = num_heads;
+  a.splits = p->attn_max_splits;
+  const int tiles = (a.K + kTile - 1) / kTile;
+  a.rows_per_split = ((tiles + a.splits - 1) / a.splits) * kTile;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = hs_stream(stream);
+  dim3 grid(2 * a.splits, p->d.num_requests);
+  mla_decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+  HS_CUDA_TRY(cudaGetLastError());
+  if (a.splits > 1) {
+    merge_splits_kernel<<<dim3(num_heads, p->d.num_requests), 128, 0, s>>>(
+        p->attn_o, p->attn_ml, a.splits, num_heads, a.out, lse);
+    HS_CUDA_TRY(cudaGetLastError());
+  }
+  return HS_OK;
 }

@@ -37,6 +37,24 @@ __global__ void offload_page_kernel(const uint4* __restrict__ kv_pool, uint4* __
 
 __global__ void unmap_page_kernel(int32_t* page_table, int64_t idx) { page_table[idx] = -1; }
 
+// Streaming copy from mapped pinned host memory into device memory by SM loads
+// (the same access path RESOLVE uses for miss rows), 4 independent 16-byte
+// loads in flight per thread.
+__global__ void __launch_bounds__(512) host_read_kernel(const uint4* __restrict__ src, int64_t n,
+                                                        uint4* __restrict__ dst) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n; i += 4 * stride) {
+    const uint4 a = __ldcs(src + i), b = __ldcs(src + i + stride);
+    const uint4 c = __ldcs(src + i + 2 * stride), d = __ldcs(src + i + 3 * stride);
+    dst[i] = a;
+    dst[i + stride] = b;
+    dst[i + 2 * stride] = c;
+    dst[i + 3 * stride] = d;
+  }
+  for (; i < n; i += stride) dst[i] = __ldcs(src + i);
+}
+
 }  // namespace
 
 extern "C" hs_status hs_offload_prefix(hs_pool* p, int32_t req, int32_t page, void* main_stream,
@@ -69,6 +87,21 @@ extern "C" hs_status hs_commit_offload(hs_pool* p, int32_t req, int32_t page, vo
   cudaStream_t ms = hs_stream(main_stream);
   HS_CUDA_TRY(cudaStreamWaitEvent(ms, reinterpret_cast<cudaEvent_t>(done_event), 0));
   unmap_page_kernel<<<1, 1, 0, ms>>>(p->page_table, (int64_t)req * p->d.max_pages + page);
+  HS_CUDA_TRY(cudaGetLastError());
+  return HS_OK;
+}
+
+extern "C" hs_status hs_host_read(const void* host_device_ptr, int64_t bytes, void* dst,
+                                  void* stream) {
+  if (!host_device_ptr || !dst || bytes < 0 || (bytes & 15) ||
+      (reinterpret_cast<uintptr_t>(host_device_ptr) & 15) || (reinterpret_cast<uintptr_t>(dst) & 15))
+    return HS_ERR_INVALID;
+  if (bytes == 0) return HS_OK;
+  int dev = 0, sms = 0;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  host_read_kernel<<<sms * 4, 512, 0, hs_stream(stream)>>>(
+      static_cast<const uint4*>(host_device_ptr), bytes / 16, static_cast<uint4*>(dst));
   HS_CUDA_TRY(cudaGetLastError());
   return HS_OK;
 }

@@ -216,3 +216,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
 }
 
 }  // namespace hs_ptx
+
+namespace hs_ptx {
+// Bulk copy global -> this CTA's shared memory, completing `bytes` of
+// transaction count on a local mbarrier (size a multiple of 16).
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst_smem, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_smem),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+}  // namespace hs_ptx

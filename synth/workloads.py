@@ -56,6 +56,7 @@ class Workload:
     appends_per_step: int = 0
     P: int = PAGE_TOKENS
     zipf_s: float = 1.1
+    req_base: int = 0               # generator id of request 0 (replicas use disjoint ids)
 
     # ---- derived scenario -------------------------------------------------
     def append_schedule(self) -> list:
@@ -125,7 +126,7 @@ class Workload:
 
     def trace(self, r: int) -> np.ndarray:
         """[steps, L, K] top-K positions of request r."""
-        return _trace(self.seed, r, self.K, self.L, self.steps,
+        return _trace(self.seed, self.req_base + r, self.K, self.L, self.steps,
                       self.ctx_per_step()[:, r].astype(np.int32), self.reuse,
                       self.zipf_frac, self.zipf_s, self.layer_share)
 

@@ -291,3 +291,15 @@ def test_graph_capture_replays_with_device_step():
         np.testing.assert_array_equal(d_out.cpu().numpy()[0], ref)
     assert int(pool.step.item()) == w.steps
     pool.close()
+
+
+def test_host_read_copies_mapped_host_memory():
+    pool, o = _small_pool(8, 64, 64, 4096)
+    n = 4096 * W.ROW_BYTES
+    dst = torch.empty(n, dtype=torch.uint8, device="cuda")
+    hs.hs_host_read(int(pool.raw.host_pool_device), n, dst)
+    torch.cuda.synchronize()
+    assert np.array_equal(dst.cpu().numpy(), pool.host_pool[0, :4096].view(np.uint8).reshape(-1))
+    with pytest.raises(hs.HsError):
+        hs.hs_host_read(int(pool.raw.host_pool_device) + 8, 64, dst)   # misaligned
+    pool.close()
