@@ -66,6 +66,7 @@ typedef enum {
 #define HS_DEV_ERR_CAPACITY 4  /* misses exceeded the slots not used this step */
 #define HS_DEV_ERR_BLOCK 8     /* page table / row id names a block outside the pool */
 #define HS_DEV_ERR_WAIT 16     /* an in-kernel bounded wait gave up */
+#define HS_DEV_ERR_INTERNAL 32 /* a kernel found its own launch set-up unusable and did nothing */
 
 typedef struct {
   int32_t num_requests;    /* R */

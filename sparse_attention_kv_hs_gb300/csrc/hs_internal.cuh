@@ -33,6 +33,7 @@ struct hs_pool {
   float* attn_o;    // [R][max_splits][128][512]
   float* attn_ml;   // [R][max_splits][128] lse
   int attn_max_splits;
+  void* attn_kv_maps;  // host array of one TMA tensor map per layer (CUtensorMap)
 
   cudaEvent_t order_event;  // orders offload copies after main-stream work
   int64_t* host_off_mirror; // host copy of host_off (set-up calls only)
@@ -51,6 +52,7 @@ hs_status hs_launch_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_laye
                             const int32_t* topk, const int32_t* d_step, int32_t* out_rows,
                             int32_t* miss_count, int32_t* miss_log, cudaStream_t stream);
 hs_status hs_attn_workspace_init(hs_pool* pool);
+void hs_attn_workspace_free(hs_pool* pool);
 // Shared memory the RESOLVE kernel needs for these sizes; sets the kernel's
 // dynamic shared-memory limit (call once per pool, outside stream capture).
 hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes);

@@ -12,27 +12,32 @@
 // Work split.  The fp32 output accumulator O (128 heads x 512) fills a whole
 // SM's tensor memory, so each (request, split-of-K) is handled by a CTA pair
 // (a cluster of 2):
-//   CTA 0 ("score"): Q lives in tensor memory (the A operand), 64-row KV tiles
-//     are staged in shared memory by cp.async, S = Q K^T (M=128, N=64, K=576)
-//     goes to a double-buffered TMEM accumulator, 4 warps run the online
-//     softmax (one thread per head) and write P as two bf16 parts (hi + lo,
-//     so P carries ~16 bits: bf16 P alone would cost ~1e-3 relative error)
-//     which one bulk copy sends into CTA 1's shared memory.
-//   CTA 1 ("value"): stages the V part (first 512 columns) of the same rows
-//     and accumulates O += P_hi V + P_lo V (M=128, N=256 x 2).  Its 4 epilogue
-//     warps rescale O when the running max moved (lazily: only when it grew by
-//     more than 2^8, so the rescale is rare and off the common path) and write
-//     the normalised output.
-// Q reaches CTA 0 by one bulk copy (then TMEM), each split's row ids are
-// staged in shared memory once, and every hand-off is an mbarrier.
-// With several splits per request, each pair writes a normalised fp32 partial
-// and its log-sum-exp; a small merge kernel combines them.
+//   CTA 0 ("score"): Q lives in tensor memory (the A operand); 64-row KV
+//     tiles are gathered by TMA (tile::gather4, 4 rows per instruction, 128B
+//     swizzle); S = Q K^T (M=128, N=64, K=576) goes to a double-buffered TMEM
+//     accumulator; 4 warps run the online softmax (one thread per head) and
+//     write P as two bf16 parts (hi + lo, so P carries ~16 bits: bf16 P alone
+//     would cost ~1e-3 relative error), which one bulk copy sends into CTA 1.
+//   CTA 1 ("value"): gathers the V part (first 512 columns) of the same rows
+//     the same way and accumulates O += P_hi V + P_lo V (M=128, N=256 x 2, V
+//     as an MN-major operand).  Its 4 epilogue warps rescale O when the
+//     running max moved (lazily: only when it grew by more than 2^8, so the
+//     rescale is rare and off the common path) and write the normalised output.
+// Q reaches CTA 0 by TMA (swizzled, then TMEM), each split's row ids are staged
+// in shared memory once, MMA descriptors are computed once and advanced by
+// constants, and every hand-off is an mbarrier.  With several splits per
+// request, each pair writes a normalised fp32 partial and its log-sum-exp; a
+// small merge kernel combines them.
 //
 // Every wait is bounded: a wait that times out sets HS_DEV_ERR_WAIT in the
 // pool's error word and the CTA winds down (no further MMAs), frees its tensor
 // memory and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <math.h>
+
+#include <new>
 
 #include "hs_internal.cuh"
 #include "sm100_ptx.cuh"
@@ -46,41 +51,44 @@ constexpr int kD = 576;            // row width (latent 512 + rope 64)
 constexpr int kDV = 512;           // value width
 constexpr int kTile = 64;          // KV rows per tile
 constexpr int kStages = 2;         // KV tile ring depth
-constexpr int kThreads = 256;
-constexpr int kLoadWarps = 3;      // warps 1..3
-constexpr int kLoaders = kLoadWarps * 32;
-constexpr int kCoreD = kD / 8;     // 72 core-matrix columns per row group (score tile)
-constexpr int kCoreV = kDV / 8;    // 64 (value tile)
+constexpr int kThreads = 384;
+constexpr int kLoadWarps = 7;      // warps 1..7 issue the TMA row gathers
+constexpr int kMathWarp0 = 8;      // warps 8..11: softmax (CTA 0) / rescale + epilogue (CTA 1)
+constexpr int kCbK = kD / 64;      // 9 swizzled 128-byte column blocks per K row
+constexpr int kCbV = kDV / 64;     // 8 for V
 
-constexpr uint32_t kStageBytes = kTile * kD * 2;          // 73728
-constexpr uint32_t kPBytes = kHeads * kTile * 2;          // 16384 per part
-constexpr uint32_t kPMetaBytes = 528;                     // alpha[128] floats + 4 flag words
-constexpr uint32_t kPCopyBytes = 2 * kPBytes + kPMetaBytes;   // 33296 (multiple of 16)
-constexpr uint32_t kPBufBytes = 2 * kPBytes + 1024;       // 33792
+constexpr uint32_t kBlockBytes = kTile * 128;              // one column block of a tile: 8192
+constexpr uint32_t kStageBytes = kCbK * kBlockBytes;       // 73728
+constexpr uint32_t kQBlockBytes = kHeads * 128;            // 16384
+constexpr uint32_t kPBytes = kHeads * kTile * 2;           // 16384 per part
+constexpr uint32_t kPMetaBytes = 528;                      // alpha[128] floats + 4 flag words
+constexpr uint32_t kPCopyBytes = 2 * kPBytes + kPMetaBytes;    // 33296 (multiple of 16)
+constexpr uint32_t kPBufBytes = 2 * kPBytes + 1024;        // 33792
 
 // Shared-memory layout, identical offsets in both CTAs of a pair (the bulk
-// copy and remote barrier operations address the peer by offset).
+// copy and remote barrier operations address the peer by offset).  Swizzled
+// regions are 1024-byte aligned.
 constexpr int kMaxSplitRows = 2048;  // row ids of one split, staged in shared memory
-constexpr uint32_t OFF_STAGE = 0;    // CTA 0 first holds Q here (<= 147456 B)
+constexpr uint32_t OFF_STAGE = 0;    // CTA 0 first holds Q here (9 x 16384 B)
 constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // 147456
 constexpr uint32_t OFF_ML = OFF_P + 2 * kPBufBytes;            // 215040: m[128], l[128]
 constexpr uint32_t OFF_RID = OFF_ML + 1024;                    // 216064: int32 [2048]
 constexpr uint32_t OFF_BAR = OFF_RID + 4 * kMaxSplitRows;      // 224256
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64;                 // 224576
-static_assert(kHeads * kD * 2 <= kStages * kStageBytes, "Q must fit the stage region");
+static_assert(kCbK * kQBlockBytes <= kStages * kStageBytes, "Q must fit the stage region");
 
 // barrier indices (8 bytes each at OFF_BAR)
 enum {
-  B_KV_FULL = 0,     // [2] loaders -> MMA (both CTAs: K tile / V tile)
+  B_KV_FULL = 0,     // [2] TMA complete_tx -> MMA (both CTAs: K tile / V tile)
   B_KV_EMPTY = 2,    // [2] MMA commit -> loaders
   B_S_FULL = 4,      // [2] score MMA commit -> softmax
   B_S_EMPTY = 6,     // [2] softmax -> score MMA
   B_P_EMPTY = 8,     // [2] (CTA 0) value MMA commit (multicast) -> softmax
-  B_Q_SMEM = 10,     // (CTA 0) bulk copy of Q landed in shared memory
-  B_Q_READY = 11,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loaders
+  B_Q_SMEM = 10,     // (CTA 0) TMA of Q landed in shared memory
+  B_Q_READY = 11,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loader
   B_P_FULL = 12,     // [2] (CTA 1) bulk copy complete_tx -> value MMA
-  B_RID = 14,        // loaders staged this split's row ids
+  B_RID = 14,        // loader warp staged this split's row ids
   B_CORR_REQ = 15,   // (CTA 1) value MMA -> rescale warps
   B_CORR_DONE = 16,  // (CTA 1) rescale warps -> value MMA
   B_MMA_IDLE = 17,   // (CTA 1) commit: earlier P.V MMAs finished
@@ -96,21 +104,19 @@ constexpr uint32_t TM_Q = 0;     // CTA 0: Q, 288 columns (bf16 pairs)
 constexpr uint32_t TM_S = 288;   // CTA 0: S, 2 x 64 columns
 constexpr uint32_t TM_O = 0;     // CTA 1: O, 512 columns
 
-constexpr uint32_t kIdescS = idesc_bf16(128, kTile, false, false);  // K-major A (TMEM), K-major B
-constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // K-major A, MN-major B
+constexpr uint32_t kIdescS = idesc_bf16(128, kTile, false, false);  // A (TMEM), B K-major
+constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // A K-major, B MN-major
 
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before giving up
 
 struct AttnArgs {
-  const uint16_t* q;        // [R][H][576]
   const int32_t* row_ids;   // [R][K]
-  const uint16_t* kv;       // layer base [rows][576]
   uint16_t* out;            // [R][H][512] bf16 (splits == 1)
   float* lse;               // [R][H] or null (splits == 1)
   float* ws_o;              // [R][splits][128][512] (splits > 1)
   float* ws_lse;            // [R][splits][128]
   int32_t* error_word;
-  int64_t rows_in_layer;
+  int32_t rows_in_layer;    // also the out-of-range row coordinate (TMA fills zeros)
   int32_t K, H, splits, rows_per_split;
   float scale_log2;         // scale * log2(e)
 };
@@ -164,33 +170,47 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Stage one 64-row tile (row ids already validated, -1 = zero row), `ncore`
-// 16-byte core columns per row, into the no-swizzle K-major core-matrix
-// layout (row group rb, core column cb at (rb*ncore + cb)*128, row%8 at +16).
-// Each warp instruction moves 8 rows x 4 core columns = 4 whole core matrices.
-__device__ __forceinline__ void load_tile(uint32_t stage, const uint16_t* kv,
-                                          const int32_t* s_rid_tile, int ncore, int lwarp,
-                                          int lane) {
-  const int quads = ncore / 4;
-  const int sub = lane & 7, cq = lane >> 3;
-  int item = 0;  // work items (row group, quad of core columns) dealt round-robin to the warps
-#pragma unroll
-  for (int rb = 0; rb < 8; ++rb) {
-    const int32_t r = s_rid_tile[rb * 8 + sub];
-    const uint16_t* row = r >= 0 ? kv + (int64_t)r * kD : kv;
-    const uint32_t src_bytes = r >= 0 ? 16u : 0u;
-    const uint32_t dst_row = stage + (uint32_t)(rb * ncore * 128 + sub * 16);
-    int q = (lwarp - item % kLoadWarps + kLoadWarps) % kLoadWarps;
-    for (; q < quads; q += kLoadWarps) {
-      const int cb = q * 4 + cq;
-      cp_async_16(dst_row + (uint32_t)(cb * 128), r >= 0 ? row + cb * 8 : kv, src_bytes);
-    }
-    item += quads;
-  }
+// Shared-memory descriptor of a 128B-swizzled operand (atoms of 8 rows x 128 B).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(addr, lbo, sbo) | ((uint64_t)2 << 61);
+}
+
+// TMA: 4 rows (y0..y3) x 64 columns from x, into 512 swizzled bytes at dst.
+// A row coordinate past the tensor reads zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0,
+                                            int y1, int y2, int y3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+// (unused: both CTAs gather their own rows, see the loader role)
+// Same 4 rows, delivered to the same shared-memory offset (and completing
+// bytes on the same barrier offset) in every CTA of cta_mask.
+__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const CUtensorMap* map, int x, int y0,
+                                               int y1, int y2, int y3, uint32_t bar,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+// TMA: one box (64 columns x box rows) from (x, y) into dst.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const AttnArgs a) {
+    mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map,
+                      const __grid_constant__ CUtensorMap q_map, const AttnArgs a) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + OFF_BAR;
@@ -213,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- set-up: barriers, tensor memory ---------------------------------
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_KV_FULL + i), kLoaders);
+      mbar_init(bar(B_KV_FULL + i), 1);
       mbar_init(bar(B_KV_EMPTY + i), 1);
       mbar_init(bar(B_S_FULL + i), 1);
       mbar_init(bar(B_S_EMPTY + i), 128);
@@ -223,13 +243,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_Q_SMEM), 1);
     mbar_init(bar(B_Q_READY), 128);
-    mbar_init(bar(B_RID), kLoaders);
+    mbar_init(bar(B_RID), 32);
     mbar_init(bar(B_CORR_REQ), 1);
     mbar_init(bar(B_CORR_DONE), 128);
     mbar_init(bar(B_MMA_IDLE), 1);
     mbar_init(bar(B_ML_FULL), 128);
     mbar_init(bar(B_FINAL), 1);
-    *abort_flag = 0;
+    // swizzled TMA destinations and descriptors assume a 1024-byte aligned base
+    *abort_flag = (sbase & 1023u) ? 1 : 0;
+    if (sbase & 1023u) atomicOr(a.error_word, HS_DEV_ERR_INTERNAL);
     *corr_tile = 0;
     *corr_exit = 0;
     fence_mbar_init_cluster();
@@ -246,41 +268,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   int err = 0;
 
   if (warp >= 1 && warp <= kLoadWarps) {
-    // ================= loaders (both CTAs) =================
-    const int lt = tid - 32, lwarp = warp - 1;
-    if (rank == 0 && lt == 0) {  // Q[r] (H x 576 bf16, contiguous) -> shared memory
-      const uint32_t qbytes = (uint32_t)a.H * kD * 2;
-      mbar_arrive_expect_tx(bar(B_Q_SMEM), qbytes);
-      bulk_copy_g2s(sbase + OFF_STAGE, a.q + (int64_t)r * a.H * kD, qbytes, bar(B_Q_SMEM));
+    // ================= loader warps (both CTAs): TMA issue =================
+    // Each CTA gathers its own copy of the rows (CTA 0: all 9 column blocks,
+    // CTA 1: the 8 value blocks), so a stage is released by that CTA's MMA
+    // alone.  The row gathers are spread over 7 warps: TMA issue throughput
+    // grows with the number of issuing warps.
+    const int lw = warp - 1;
+    if (rank == 0 && lw == 0 && lane == 0 && !*abort_flag) {  // Q[r] (128 rows) -> smem
+      mbar_arrive_expect_tx(bar(B_Q_SMEM), kCbK * kQBlockBytes);
+      for (int cb = 0; cb < kCbK; ++cb)
+        tma_load_2d(sbase + OFF_STAGE + cb * kQBlockBytes, &q_map, cb * 64, r * a.H,
+                    bar(B_Q_SMEM));
     }
-    // this split's row ids -> shared memory, validated once (-1 = no row)
-    const int32_t* g_rows = a.row_ids + (int64_t)r * a.K;
-    for (int i = lt; i < n_tiles * kTile; i += kLoaders) {
-      const int j = j_begin + i;
-      int32_t v = j < j_end ? __ldg(g_rows + j) : -1;
-      if (v < -1 || v >= a.rows_in_layer) {
-        err |= HS_DEV_ERR_BLOCK;
-        v = -1;
+    if (lw == 0) {  // this split's row ids -> shared memory, validated once (-1 = no row)
+      const int32_t* g_rows = a.row_ids + (int64_t)r * a.K;
+      for (int i = lane; i < n_tiles * kTile; i += 32) {
+        const int j = j_begin + i;
+        int32_t v = j < j_end ? __ldg(g_rows + j) : -1;
+        if (v < -1 || v >= a.rows_in_layer) {
+          err |= HS_DEV_ERR_BLOCK;
+          v = -1;
+        }
+        s_rid[i] = v;
       }
-      s_rid[i] = v;
+      __syncwarp();
+      mbar_arrive(bar(B_RID));
     }
-    asm volatile("bar.sync 2, 96;" ::: "memory");  // the 3 loader warps, unconditionally
-    mbar_arrive(bar(B_RID));
-    const int ncore = rank == 0 ? kCoreD : kCoreV;
+    bool ok = wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word);
     // CTA 0: Q occupies the stage region until it has moved to TMEM
-    bool ok = rank == 0 ? wait_bar(bar(B_Q_READY), 0, abort_flag, a.error_word) : true;
+    if (rank == 0) ok = ok && wait_bar_warp(bar(B_Q_READY), 0, abort_flag, a.error_word);
+    const int ncb = rank == 0 ? kCbK : kCbV;
+    const int n_items = ncb * (kTile / 4);  // (column block, 4-row group) pairs
     for (int t = 0; ok && t < n_tiles; ++t) {
       const int s = t % kStages;
       const uint32_t ph = (uint32_t)(t / kStages) & 1u;
-      if (!wait_bar(bar(B_KV_EMPTY + s), ph ^ 1u, abort_flag, a.error_word)) break;
-      load_tile(sbase + OFF_STAGE + s * kStageBytes, a.kv, s_rid + t * kTile, ncore, lwarp, lane);
-      cp_async_arrive(bar(B_KV_FULL + s));
+      if (!wait_bar_warp(bar(B_KV_EMPTY + s), ph ^ 1u, abort_flag, a.error_word)) break;
+      if (lw == 0 && lane == 0)
+        mbar_arrive_expect_tx(bar(B_KV_FULL + s), (uint32_t)ncb * kBlockBytes);
+      if (lane < kTile / 4) {
+        const int32_t* rid = s_rid + t * kTile + 4 * lane;  // lane g moves rows 4g .. 4g+3
+        const int y0 = rid[0] >= 0 ? rid[0] : a.rows_in_layer;
+        const int y1 = rid[1] >= 0 ? rid[1] : a.rows_in_layer;
+        const int y2 = rid[2] >= 0 ? rid[2] : a.rows_in_layer;
+        const int y3 = rid[3] >= 0 ? rid[3] : a.rows_in_layer;
+        const uint32_t dst = sbase + OFF_STAGE + s * kStageBytes + lane * 512;
+        for (int item = lw * 16 + lane; item < n_items; item += kLoadWarps * 16) {
+          const int cb = item >> 4;
+          tma_gather4(dst + cb * kBlockBytes, &kv_map, cb * 64, y0, y1, y2, y3, bar(B_KV_FULL + s));
+        }
+      }
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == 0) {
     // ================= MMA issuer =================
     if (lane == 0) {
       if (rank == 0) {
+        // B = K tile, K-major, 128B swizzle: column block cb at +cb*8192, K step
+        // kk at +(kk%4)*32 inside the block; 8-row groups 1024 B apart
+        const uint64_t kdesc0 = desc_sw128(sbase + OFF_STAGE, 16, 1024);
         if (wait_bar(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
           tc_fence_after();
           for (int t = 0; t < n_tiles; ++t) {
@@ -289,16 +333,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!wait_bar(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
             if (!wait_bar(bar(B_S_EMPTY + b), pb ^ 1u, abort_flag, a.error_word)) break;
             tc_fence_after();
-            const uint32_t kst = sbase + OFF_STAGE + s * kStageBytes;
-#pragma unroll 4
+            const uint64_t kd = kdesc0 + ((s * kStageBytes) >> 4);
+            const uint32_t dS = tm + TM_S + b * kTile;
+#pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              mma_ts(tm + TM_S + b * kTile, tm + TM_Q + kk * 8,
-                     smem_desc(kst + kk * 256, 128, kCoreD * 128), kIdescS, kk > 0);
+              mma_ts(dS, tm + TM_Q + kk * 8,
+                     kd + (uint64_t)((((kk >> 2) * kBlockBytes) + (kk & 3) * 32) >> 4), kIdescS,
+                     kk > 0);
             mma_commit(bar(B_KV_EMPTY + s));
             mma_commit(bar(B_S_FULL + b));
           }
         }
       } else {
+        // A = P (interleaved core matrices: K step kk at +kk*256, 8-head groups
+        // 1024 B apart); B = V, MN-major, 128B swizzle: 64-column blocks
+        // 8192 B apart, 8-row groups 1024 B apart, K step kk at +kk*2048
+        const uint64_t pdesc0 = smem_desc(sbase + OFF_P, 128, 1024);
+        const uint64_t vdesc0 = desc_sw128(sbase + OFF_STAGE, kBlockBytes, 1024);
         uint32_t corr = 0;
         for (int t = 0; t < n_tiles; ++t) {
           const int s = t % kStages, b = t & 1;
@@ -306,7 +357,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(B_P_FULL + b), kPCopyBytes);
           if (!wait_bar(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
           if (!wait_bar(bar(B_P_FULL + b), pb, abort_flag, a.error_word, true)) break;
-          const uint32_t pbuf = sbase + OFF_P + b * kPBufBytes;
           const uint32_t* flags =
               reinterpret_cast<const uint32_t*>(smem + OFF_P + b * kPBufBytes + 2 * kPBytes + 512);
           if (t > 0 && (flags[0] | flags[1] | flags[2] | flags[3])) {
@@ -319,19 +369,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++corr;
           }
           tc_fence_after();
-          const uint32_t vst = sbase + OFF_STAGE + s * kStageBytes;
+          const uint64_t pd = pdesc0 + ((b * kPBufBytes) >> 4);
+          const uint64_t vd = vdesc0 + ((s * kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
-              const uint64_t adesc = smem_desc(pbuf + part * kPBytes + kk * 256, 128, 1024);
 #pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                const uint64_t bdesc =
-                    smem_desc(vst + kk * 2 * (kCoreV * 128) + half * 4096, kCoreV * 128, 128);
-                mma_ss(tm + TM_O + half * 256, adesc, bdesc, kIdescPV,
+              for (int half = 0; half < 2; ++half)
+                mma_ss(tm + TM_O + half * 256, pd + (uint64_t)((part * kPBytes + kk * 256) >> 4),
+                       vd + (uint64_t)((half * 4 * kBlockBytes + kk * 2048) >> 4), kIdescPV,
                        (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
-              }
             }
           }
           mma_commit(bar(B_KV_EMPTY + s));
@@ -344,19 +392,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       wait_bar(bar(B_FINAL), 0, abort_flag, a.error_word);
     }
     __syncwarp();
-  } else if (rank == 0) {
+  } else if (warp >= kMathWarp0 && rank == 0) {
     // ================= softmax (CTA 0, warps 4..7, one thread per head) =================
-    const int h = tid - 128;
+    const int h = tid - kMathWarp0 * 32;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = wait_bar_warp(bar(B_Q_SMEM), 0, abort_flag, a.error_word);
     if (ok) {  // Q[h] -> TMEM columns TM_Q .. TM_Q+287 (bf16 pairs), zero for padded heads
-      const uint4* qs = reinterpret_cast<const uint4*>(smem + OFF_STAGE) + h * (kD / 8);
+      // swizzled rows: column block cb holds [128 rows][128 B]; 16-byte chunk c
+      // of row h sits at chunk position c ^ (h % 8) (conflict-free reads)
+      const unsigned char* qrow = smem + OFF_STAGE + h * 128;
       for (int c0 = 0; c0 < kD / 2; c0 += 16) {
         uint32_t v[16];
+        const unsigned char* blk = qrow + (c0 / 32) * kQBlockBytes;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
+          const int c = (c0 % 32) / 4 + i;
           uint4 x = make_uint4(0, 0, 0, 0);
-          if (h < a.H) x = qs[c0 / 4 + i];
+          if (h < a.H) x = *reinterpret_cast<const uint4*>(blk + ((c ^ (h & 7)) * 16));
           v[4 * i + 0] = x.x;
           v[4 * i + 1] = x.y;
           v[4 * i + 2] = x.z;
@@ -448,9 +500,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (t < 0) continue;
       wait_bar(bar(B_P_EMPTY + (t & 1)), (uint32_t)(t >> 1) & 1u, abort_flag, a.error_word);
     }
-  } else {
+  } else if (warp >= kMathWarp0) {
     // ================= rescale + epilogue (CTA 1, warps 4..7) =================
-    const int h = tid - 128;
+    const int h = tid - kMathWarp0 * 32;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     for (uint32_t k = 0;; ++k) {  // rare: only tiles where some head's max moved
       if (!wait_bar_warp(bar(B_CORR_REQ), k & 1u, abort_flag, a.error_word)) break;
@@ -579,15 +631,53 @@ int choose_splits(int num_sms, int R, int K) {
   return s;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+hs_status get_encoder() {
+  if (g_encode) return HS_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return HS_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return HS_OK;
+}
+
+// 2-D bf16 tensor map over [rows][576], 128B swizzle, box = 64 columns x box_rows.
+hs_status encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  if (get_encoder() != HS_OK) return HS_ERR_CUDA;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  const CUresult cr = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                               dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return cr == CUDA_SUCCESS ? HS_OK : HS_ERR_INVALID;
+}
+
 }  // namespace
 
 hs_status hs_attn_workspace_init(hs_pool* p) {
   p->attn_o = nullptr;
   p->attn_ml = nullptr;
+  p->attn_kv_maps = nullptr;
   p->attn_max_splits = 0;
   if (p->d.row_elems != kD) return HS_OK;  // attention needs 576-wide rows; decode call rejects
   HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)kSmemBytes));
+  const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
+  CUtensorMap* maps = new (std::nothrow) CUtensorMap[p->d.num_layers];
+  if (!maps) return HS_ERR_OOM;
+  p->attn_kv_maps = maps;
+  for (int l = 0; l < p->d.num_layers; ++l) {
+    const void* base = static_cast<const uint16_t*>(p->kv_pool) + (int64_t)l * rows_in_layer * kD;
+    const hs_status st = encode_rows_map(&maps[l], base, (uint64_t)rows_in_layer, 1);
+    if (st != HS_OK) return st;
+  }
   const int splits = choose_splits(p->num_sms, p->d.num_requests, p->d.top_k);
   p->attn_max_splits = splits;
   if (splits > 1) {
@@ -601,26 +691,37 @@ hs_status hs_attn_workspace_init(hs_pool* p) {
   return HS_OK;
 }
 
+void hs_attn_workspace_free(hs_pool* p) {
+  cudaFree(p->attn_o);
+  cudaFree(p->attn_ml);
+  delete[] static_cast<CUtensorMap*>(p->attn_kv_maps);
+  p->attn_o = nullptr;
+  p->attn_ml = nullptr;
+  p->attn_kv_maps = nullptr;
+}
+
 extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void* q,
                                           const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
                                           float scale, void* out, float* lse, void* stream) {
   if (!p || !q || !row_ids || !out) return HS_ERR_INVALID;
   if (layer < 0 || layer >= p->d.num_layers || num_heads <= 0 || num_heads > kHeads ||
-      v_dim != kDV || p->d.row_elems != kD || !(scale > 0.f) || p->attn_max_splits < 1)
+      v_dim != kDV || p->d.row_elems != kD || !(scale > 0.f) || p->attn_max_splits < 1 ||
+      !p->attn_kv_maps)
     return HS_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
     return HS_ERR_INVALID;
   const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
+  CUtensorMap q_map;  // host-side encode only: safe inside stream capture
+  if (encode_rows_map(&q_map, q, (uint64_t)p->d.num_requests * num_heads, kHeads) != HS_OK)
+    return HS_ERR_INVALID;
   AttnArgs a;
-  a.q = static_cast<const uint16_t*>(q);
   a.row_ids = row_ids;
-  a.kv = static_cast<const uint16_t*>(p->kv_pool) + (int64_t)layer * rows_in_layer * kD;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
   a.ws_o = p->attn_o;
   a.ws_lse = p->attn_ml;
   a.error_word = p->error_word;
-  a.rows_in_layer = rows_in_layer;
+  a.rows_in_layer = (int32_t)rows_in_layer;
   a.K = p->d.top_k;
   a.H = num_heads;
   a.splits = p->attn_max_splits;
@@ -629,7 +730,8 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void*
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t s = hs_stream(stream);
   dim3 grid(2 * a.splits, p->d.num_requests);
-  mla_decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+  mla_decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(
+      static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q_map, a);
   HS_CUDA_TRY(cudaGetLastError());
   if (a.splits > 1) {
     merge_splits_kernel<<<dim3(num_heads, p->d.num_requests), 128, 0, s>>>(

@@ -68,8 +68,7 @@ void free_pool(hs_pool* p) {
   cudaFree(p->lru_order);
   cudaFree(p->step);
   cudaFree(p->error_word);
-  cudaFree(p->attn_o);
-  cudaFree(p->attn_ml);
+  hs_attn_workspace_free(p);
   if (p->order_event) cudaEventDestroy(p->order_event);
   delete[] p->host_off_mirror;
   delete p;
