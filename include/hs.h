@@ -189,6 +189,32 @@ hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, const void* q,
                                int32_t v_dim, float scale, void* out,
                                float* lse, void* stream);
 
+/* Allocation-free variant of hs_sparse_mla_decode (no counterpart on the
+ * pages: it exists for callers that cannot allocate device memory when they
+ * decode -- an engine that handed all free HBM to its KV cache at start-up, an
+ * allocator that forbids new device allocations while serving, or a plug-in
+ * that is only given raw device pointers -- and so cannot create a pool).
+ * Same computation and output as hs_sparse_mla_decode, with plain pointers:
+ *   kv_rows   device bf16 [num_rows][576]: the layer's KV rows, row ids index it
+ *   q         device bf16 [num_requests][num_heads][576]
+ *   row_ids   device int32 [num_requests][top_k] (-1 = padding; an id outside
+ *             [0, num_rows) is excluded like padding and is not reported)
+ *   out, lse  as for hs_sparse_mla_decode
+ * It calls no cudaMalloc, cudaFree or other allocating routine: its split-K
+ * scratch is a fixed device array of this library (16 MiB + 32 KiB, held by
+ * every GPU that loads the library until the process exits), big enough for
+ * 64 (request, split) partials; the call uses fewer splits to fit, and returns
+ * HS_ERR_INVALID if num_requests x ceil(top_k / 2048) > 64.  The first call on
+ * a device looks up that array's device address and sets the kernel's
+ * shared-memory limit (no allocation); make it before any stream capture.
+ * Every call shares the array, so calls whose kernels overlap on the GPU (for
+ * example on two streams) race; nothing in it needs to start at zero.  Async on
+ * `stream`. */
+hs_status hs_sparse_mla_decode_noalloc(const void* kv_rows, int64_t num_rows, const void* q,
+                                       const int32_t* row_ids, int32_t num_requests,
+                                       int32_t top_k, int32_t num_heads, int32_t v_dim,
+                                       float scale, void* out, float* lse, void* stream);
+
 /* Prefix offload: copy page `page` of request `req` (all layers, from the
  * block the page table maps it to) into its rows of the host pool.  The copy
  * is one kernel launch on `side_stream`, ordered after the work queued so far

@@ -36,6 +36,7 @@ EXPORTED = (
     "hs_set_request", "hs_map_page", "hs_load_page", "hs_resolve", "hs_gather",
     "hs_sparse_mla_decode", "hs_offload_prefix", "hs_commit_offload",
     "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
+    "hs_sparse_mla_decode_noalloc",
 )
 
 
@@ -98,6 +99,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_step_advance": [p, p],
         "hs_check_errors": [p, ctypes.POINTER(i32)],
         "hs_host_read": [p, i64, p, p],
+        "hs_sparse_mla_decode_noalloc": [p, i64, p, p, i32, i32, i32, i32, f32, p, p, p],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -207,6 +209,17 @@ def hs_sparse_mla_decode(pool: int, layer: int, q, row_ids, num_heads: int, v_di
     _check(load().hs_sparse_mla_decode(pool, layer, _addr(q), _addr(row_ids), num_heads, v_dim,
                                        scale, _addr(out), _addr(lse), _stream(stream)),
            "hs_sparse_mla_decode")
+
+
+def hs_sparse_mla_decode_noalloc(kv_rows, num_rows: int, q, row_ids, num_requests: int,
+                                 top_k: int, num_heads: int, v_dim: int, scale: float, out,
+                                 lse=None, stream=None) -> None:
+    """Decode attention without any device allocation (scratch is a fixed
+    library array); for callers that cannot allocate when they decode."""
+    _check(load().hs_sparse_mla_decode_noalloc(_addr(kv_rows), num_rows, _addr(q), _addr(row_ids),
+                                               num_requests, top_k, num_heads, v_dim, scale,
+                                               _addr(out), _addr(lse), _stream(stream)),
+           "hs_sparse_mla_decode_noalloc")
 
 
 def hs_offload_prefix(pool: int, req: int, page: int, main_stream, side_stream, done_event) -> None:

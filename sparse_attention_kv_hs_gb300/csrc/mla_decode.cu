@@ -740,3 +740,107 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void*
   }
   return HS_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the decode call.
+//
+// Some callers cannot allocate device memory at the point where they decode:
+// an engine that reserved all free HBM for its KV cache up front, code running
+// under an allocator that forbids new device allocations once serving starts,
+// or a plug-in that only receives raw device pointers from its host.  For
+// them, hs_sparse_mla_decode_noalloc() takes the KV rows, queries, row ids and
+// outputs as plain pointers and keeps its split-K scratch (per-split partial
+// outputs and their log-sum-exp) in the fixed device array below, which every
+// GPU that loads this library holds until the process exits.  It calls no
+// cudaMalloc, cudaFree or allocating library routine.
+//
+// Capacity: partials for at most kNoAllocMaxUnits (request, split) pairs.  The
+// call picks splits = min(its usual choice, kNoAllocMaxUnits / R), and rejects
+// the call (HS_ERR_INVALID) when even the fewest splits the kernel allows
+// (ceil(K / 2048)) need more.  With one split no scratch is used at all.
+// Every call overwrites the scratch it uses before reading it, so nothing has
+// to start at zero; calls whose kernels overlap on the GPU (e.g. on two
+// streams) share the array and race.
+constexpr int kNoAllocMaxUnits = 64;  // 64 x 128 x 512 fp32 = 16 MiB (+ 32 KiB lse)
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocMaxUnits * kHeads * (kDV + 1)];
+static __device__ int32_t g_noalloc_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+float* g_noalloc_ptr[kMaxDevices];       // device address of the scratch, per device
+int32_t* g_noalloc_err_ptr[kMaxDevices];
+int g_noalloc_sms[kMaxDevices];
+
+// Once per device, with that device current: resolve the scratch's device
+// address (in host code the array's name is only a stand-in, not an address)
+// and raise the kernel's shared-memory limit.
+hs_status noalloc_setup(int dev) {
+  if (g_noalloc_ptr[dev]) return HS_OK;
+  void* scratch = nullptr;
+  void* errw = nullptr;
+  HS_CUDA_TRY(cudaGetSymbolAddress(&scratch, g_noalloc_scratch));
+  HS_CUDA_TRY(cudaGetSymbolAddress(&errw, g_noalloc_error_word));
+  HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kSmemBytes));
+  int sms = 0;
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  g_noalloc_sms[dev] = sms;
+  g_noalloc_err_ptr[dev] = static_cast<int32_t*>(errw);
+  g_noalloc_ptr[dev] = static_cast<float*>(scratch);
+  return HS_OK;
+}
+}  // namespace
+
+extern "C" hs_status hs_sparse_mla_decode_noalloc(const void* kv_rows, int64_t num_rows,
+                                                  const void* q, const int32_t* row_ids,
+                                                  int32_t num_requests, int32_t top_k,
+                                                  int32_t num_heads, int32_t v_dim, float scale,
+                                                  void* out, float* lse, void* stream) {
+  if (!kv_rows || !q || !row_ids || !out) return HS_ERR_INVALID;
+  if (num_rows <= 0 || num_rows > INT32_MAX || num_requests <= 0 || top_k <= 0 ||
+      num_heads <= 0 || num_heads > kHeads || v_dim != kDV || !(scale > 0.f))
+    return HS_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(kv_rows) & 15) || (reinterpret_cast<uintptr_t>(q) & 15) ||
+      (reinterpret_cast<uintptr_t>(out) & 15))
+    return HS_ERR_INVALID;
+  const int tiles = (top_k + kTile - 1) / kTile;
+  const int min_splits = (tiles * kTile + kMaxSplitRows - 1) / kMaxSplitRows;
+  if (min_splits > 1 && (int64_t)num_requests * min_splits > kNoAllocMaxUnits)
+    return HS_ERR_INVALID;  // the fixed scratch cannot hold this many partials
+  int dev = 0;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return HS_ERR_INVALID;
+  const hs_status st = noalloc_setup(dev);
+  if (st != HS_OK) return st;
+  int splits = choose_splits(g_noalloc_sms[dev], num_requests, top_k);
+  if (splits > 1 && (int64_t)num_requests * splits > kNoAllocMaxUnits)
+    splits = kNoAllocMaxUnits / num_requests;
+  if (splits < min_splits) splits = min_splits;
+  CUtensorMap kv_map, q_map;  // host-side encodes only
+  if (encode_rows_map(&kv_map, kv_rows, (uint64_t)num_rows, 1) != HS_OK ||
+      encode_rows_map(&q_map, q, (uint64_t)num_requests * num_heads, kHeads) != HS_OK)
+    return HS_ERR_INVALID;
+  float* scratch = g_noalloc_ptr[dev];
+  AttnArgs a;
+  a.row_ids = row_ids;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.ws_o = scratch;
+  a.ws_lse = scratch + (size_t)kNoAllocMaxUnits * kHeads * kDV;
+  a.error_word = g_noalloc_err_ptr[dev];
+  a.rows_in_layer = (int32_t)num_rows;
+  a.K = top_k;
+  a.H = num_heads;
+  a.splits = splits;
+  a.rows_per_split = ((tiles + splits - 1) / splits) * kTile;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = hs_stream(stream);
+  mla_decode_kernel<<<dim3(2 * splits, num_requests), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
+  HS_CUDA_TRY(cudaGetLastError());
+  if (splits > 1) {
+    merge_splits_kernel<<<dim3(num_heads, num_requests), 128, 0, s>>>(a.ws_o, a.ws_lse, splits,
+                                                                      num_heads, a.out, lse);
+    HS_CUDA_TRY(cudaGetLastError());
+  }
+  return HS_OK;
+}
