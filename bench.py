@@ -61,6 +61,27 @@ def parse_args(argv=None):
 
 # ----------------------------------------------------------------- helpers
 
+def replica_request_base(rank: int, requests_per_replica: int) -> int:
+    """Generator id of a replica's first request: replicas serve disjoint
+    requests (units are independent, so the path shards with no exchange)."""
+    return rank * requests_per_replica
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The slowest rank's time (every rank gets it)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_rate(units_per_rank_step: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank's units over the slowest rank's time."""
+    return world * steps * units_per_rank_step / (elapsed_ms * 1e-3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -288,7 +309,7 @@ def run_ours(args):
     lib = hs.load()
 
     w = W.make(args.workload)
-    w.req_base = rank * w.R          # each replica serves its own requests
+    w.req_base = replica_request_base(rank, w.R)
     steps_total = args.warmup + args.steps
     topk_h, q_h = build_inputs(w, steps_total)
     scen = W.Scenario.build(w)
@@ -361,11 +382,7 @@ def run_ours(args):
     t_end.record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop() if clocks else None
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if dist is not None:
-        tt = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
     res_ms = sum(e[0][l].elapsed_time(e[1][l]) for e in evs for l in range(L))
     att_ms = sum(e[1][l].elapsed_time(e[2][l]) for e in evs for l in range(L))
     errs = hs.hs_check_errors(ph)
@@ -374,8 +391,8 @@ def run_ours(args):
     misses = int(cnt_d[args.warmup:].sum().item())
 
     rows_per_step = L * R * K
-    value = world * args.steps * rows_per_step / (elapsed_ms * 1e-3)
-    tok_s = world * args.steps * R / (elapsed_ms * 1e-3)
+    value = weak_scaling_rate(rows_per_step, args.steps, world, elapsed_ms)
+    tok_s = weak_scaling_rate(R, args.steps, world, elapsed_ms)
     n_launch_res = args.steps * L
     res_avg_s = res_ms * 1e-3 / n_launch_res
     att_avg_s = att_ms * 1e-3 / n_launch_res
@@ -521,16 +538,12 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
         step(args.warmup + i)
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if dist is not None:
-        tt = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(a.elapsed_time(b), dist, dev)
     if hs.hs_check_errors(pool.handle):
         raise RuntimeError("device error word set in the e2e run")
     h2d = L * R * K * 4 + (L * R * H * W.ROW_ELEMS * 2 if attention else 0)
     d2h = (L * R * H * (W.V_DIM * 2 + 4)) if attention else R * K * W.ROW_BYTES
-    return {"value": world * steps * L * R * K / (ms * 1e-3), "unit": "rows/s",
+    return {"value": weak_scaling_rate(L * R * K, steps, world, ms), "unit": "rows/s",
             "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 

@@ -34,7 +34,9 @@
  *   page_table    device int32 [R][max_pages]: block id, or -1 = host only
  *   LRU metadata  device int32 [L][R][B] slot_pos (-1 = empty),
  *                 slot_stamp (step of last use, -1 = never), lru_order (slots
- *                 sorted by (stamp, slot) ascending)
+ *                 sorted by (stamp, slot) ascending); plus an internal
+ *                 position -> slot array [L][host_tokens] that RESOLVE keeps
+ *                 consistent (modify LRU state only through this API)
  *
  * Errors.  Argument errors are returned synchronously.  Errors found on the
  * device (bad indices in caller data) never trap: the kernel writes row id
@@ -122,7 +124,9 @@ hs_status hs_pool_reset(hs_pool* pool, void* stream);
 
 /* Set a request's current context length and its first row in the host pool.
  * Async on `stream`, graph-capturable.  HS_ERR_INVALID if req is out of range,
- * ctx_len > max_pages * P or host_off + ctx_len > host_tokens. */
+ * ctx_len > max_pages * P or host_off + ctx_len > host_tokens.  A request's
+ * host_off must not change while its units hold hot rows (hs_pool_reset
+ * first); growing ctx_len is always allowed. */
 hs_status hs_set_request(hs_pool* pool, int32_t req, int32_t ctx_len,
                          int64_t host_off, void* stream);
 

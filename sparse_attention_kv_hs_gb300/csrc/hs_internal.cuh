@@ -26,6 +26,7 @@ struct hs_pool {
   int32_t* slot_pos;    // [L][R][B]
   int32_t* slot_stamp;  // [L][R][B]
   int32_t* lru_order;   // [L][R][B]
+  int32_t* inv;         // [L][host_tokens]: hot slot holding each host row, or -1
   int32_t* step;        // scalar
   int32_t* error_word;  // scalar
 

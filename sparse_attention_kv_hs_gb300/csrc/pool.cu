@@ -29,6 +29,21 @@ __global__ void reset_kernel(int32_t* slot_pos, int32_t* slot_stamp, int32_t* lr
   }
 }
 
+// Clear the position -> slot entries of every occupied slot (before the slots
+// themselves are emptied), so the inverse array stays consistent.
+__global__ void clear_inverse_kernel(const int32_t* slot_pos, int32_t* inv, const int64_t* host_off,
+                                     int32_t R, int32_t B, int64_t units, int64_t host_tokens) {
+  const int64_t n = units * B;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t p = slot_pos[i];
+    if (p < 0) continue;
+    const int64_t u = i / B;
+    const int64_t l = u / R, r = u % R;
+    inv[l * host_tokens + host_off[r] + p] = -1;
+  }
+}
+
 __global__ void init_tables_kernel(int32_t* page_table, int64_t n_pt, int32_t* hot_block,
                                    int32_t R, int32_t hot_per_req, int32_t* ctx_len,
                                    int64_t* host_off) {
@@ -66,6 +81,7 @@ void free_pool(hs_pool* p) {
   cudaFree(p->slot_pos);
   cudaFree(p->slot_stamp);
   cudaFree(p->lru_order);
+  cudaFree(p->inv);
   cudaFree(p->step);
   cudaFree(p->error_word);
   hs_attn_workspace_free(p);
@@ -156,6 +172,11 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
   if ((st = dev_alloc(&p->slot_pos, (size_t)L * R * B)) != HS_OK) goto fail;
   if ((st = dev_alloc(&p->slot_stamp, (size_t)L * R * B)) != HS_OK) goto fail;
   if ((st = dev_alloc(&p->lru_order, (size_t)L * R * B)) != HS_OK) goto fail;
+  if ((st = dev_alloc(&p->inv, (size_t)L * d.host_tokens)) != HS_OK) goto fail;
+  if (cudaMemset(p->inv, 0xFF, sizeof(int32_t) * (size_t)L * d.host_tokens) != cudaSuccess) {
+    st = HS_ERR_CUDA;
+    goto fail;
+  }
   if ((st = dev_alloc(&p->step, 1)) != HS_OK) goto fail;
   if ((st = dev_alloc(&p->error_word, 1)) != HS_OK) goto fail;
   if ((st = hs_attn_workspace_init(p)) != HS_OK) goto fail;
@@ -209,6 +230,9 @@ extern "C" hs_status hs_pool_get_views(const hs_pool* p, hs_pool_views* v) {
 extern "C" hs_status hs_pool_reset(hs_pool* p, void* stream) {
   if (!p) return HS_ERR_INVALID;
   const int64_t units = (int64_t)p->d.num_layers * p->d.num_requests;
+  clear_inverse_kernel<<<256, 256, 0, hs_stream(stream)>>>(p->slot_pos, p->inv, p->host_off,
+                                                           p->d.num_requests, p->d.hot_slots, units,
+                                                           p->d.host_tokens);
   reset_kernel<<<256, 256, 0, hs_stream(stream)>>>(p->slot_pos, p->slot_stamp, p->lru_order,
                                                    units, p->d.hot_slots, p->step,
                                                    p->error_word);

@@ -11,8 +11,9 @@
 // decode path waits on a CPU decision (the step comes from device memory).
 //
 // Per unit, in shared memory:
-//   1. slot hash (position -> slot) built from slot_pos; selection hash
-//      (position -> first j) for repeat detection;
+//   1. selection hash (position -> first j) for repeat detection; hit
+//      detection reads the pool's persistent position -> slot array (inv),
+//      which misses keep up to date, so no per-call table is rebuilt;
 //   2. classify each j: padding / error / resident / hot hit (stamp := step) /
 //      miss; misses are numbered in j order by a block scan;
 //   3. victims: lru_order lists the slots sorted by (stamp, slot).  Slots hit
@@ -23,8 +24,14 @@
 //      slot number), which keeps lru_order sorted by (stamp, slot);
 //   4. each miss writes slot_pos/stamp/out and its host row is copied from
 //      mapped pinned host memory into the slot's pool row with 16-byte
-//      vector loads and stores, all threads of the CTA sharing the rows.
+//      vector loads and stores.
+// The copies are bound by how many host reads are in flight, which is capped
+// per SM, so a unit is served by a cluster of C CTAs (C = SMs / units, at most
+// 8): CTA 0 runs steps 1-3 and 4's metadata, the others wait at a cluster
+// barrier, fetch their share of the miss list from CTA 0's shared memory and
+// every CTA copies its share of the rows.
 #include "hs_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace {
 
@@ -45,27 +52,29 @@ struct ResolveArgs {
   int32_t* slot_pos;
   int32_t* slot_stamp;
   int32_t* lru_order;
+  int32_t* inv;  // [L][host_tokens]: slot holding host row (host_off[r] + p), or -1
   const uint4* host_pool;
   uint4* kv_pool;
   int32_t* error_word;
   int64_t host_tokens;
   int64_t blocks_per_layer;
   int32_t layer_begin, R, K, B, P, max_pages, row_vec;
-  int32_t slot_bits, sel_bits, kpt, bpt;
+  int32_t sel_bits, kpt, bpt;
+  int32_t copy_ctas;  // C: CTAs (a cluster) per unit
 };
 
 struct SmemPlan {
-  size_t slot_pos, order, slot_hash, sel_key, sel_j, miss_j, miss_p, victim, hot, flag, warp, total;
+  size_t order, sel_key, sel_j, miss_j, miss_p, victim, hot, flag, warp, ptab, total;
 };
+
+constexpr int kMaxSmemPages = 4096;  // page-table rows up to this width are staged in smem
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int slot_bits, int sel_bits) {
+__host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int sel_bits) {
   SmemPlan s;
   size_t o = 0;
-  s.slot_pos = o;  o = align16(o + sizeof(int32_t) * B);
   s.order = o;     o = align16(o + sizeof(int32_t) * B);
-  s.slot_hash = o; o = align16(o + sizeof(int32_t) * (size_t(1) << slot_bits));
   s.sel_key = o;   o = align16(o + sizeof(int32_t) * (size_t(1) << sel_bits));
   s.sel_j = o;     o = align16(o + sizeof(int32_t) * (size_t(1) << sel_bits));
   s.miss_j = o;    o = align16(o + sizeof(int32_t) * K);
@@ -74,8 +83,15 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int slot_bits
   s.hot = o;       o = align16(o + sizeof(int32_t) * (B / P));
   s.flag = o;      o = align16(o + B);
   s.warp = o;      o = align16(o + sizeof(int32_t) * (kWarps + 8));
+  s.ptab = o;      o = align16(o + sizeof(int32_t) * kMaxSmemPages);
   s.total = o;
   return s;
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint32_t hash_pos(int32_t p, int bits) {
@@ -109,12 +125,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return base + x - v;
 }
 
+// P_CT / RV_CT: compile-time page size and row width (16-byte vectors) for the
+// common shape (256, 72 = 576 bf16); 0 = take them from the arguments.
+template <int P_CT, int RV_CT>
 __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const SmemPlan sp = smem_plan(a.K, a.B, a.P, a.slot_bits, a.sel_bits);
-  int32_t* s_slot_pos = reinterpret_cast<int32_t*>(smem + sp.slot_pos);
+  const SmemPlan sp = smem_plan(a.K, a.B, a.P, a.sel_bits);
   int32_t* s_order = reinterpret_cast<int32_t*>(smem + sp.order);
-  int32_t* s_slot_hash = reinterpret_cast<int32_t*>(smem + sp.slot_hash);
   int32_t* s_sel_key = reinterpret_cast<int32_t*>(smem + sp.sel_key);
   int32_t* s_sel_j = reinterpret_cast<int32_t*>(smem + sp.sel_j);
   int32_t* s_miss_j = reinterpret_cast<int32_t*>(smem + sp.miss_j);
@@ -123,17 +140,19 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   int32_t* s_hot = reinterpret_cast<int32_t*>(smem + sp.hot);
   uint8_t* s_flag = smem + sp.flag;
   int* s_warp = reinterpret_cast<int*>(smem + sp.warp);
+  int32_t* s_ptab = reinterpret_cast<int32_t*>(smem + sp.ptab);
   int* s_err = s_warp + kWarps;
 
   const int tid = threadIdx.x;
-  const int r = blockIdx.x;
+  const int C = a.copy_ctas;
+  const uint32_t crank = C > 1 ? hs_ptx::cluster_ctarank() : 0u;
+  const int r = blockIdx.x / C;
   const int li = blockIdx.y;               // layer index within this call
   const int l = a.layer_begin + li;        // absolute layer
   const int64_t unit = (int64_t)l * a.R + r;
   const int64_t call_unit = (int64_t)li * a.R + r;
-  const int K = a.K, B = a.B, P = a.P;
+  const int K = a.K, B = a.B, P = P_CT ? P_CT : a.P;
   const int hot_per_req = B / P;
-  const int slot_mask = (1 << a.slot_bits) - 1;
   const int sel_mask = (1 << a.sel_bits) - 1;
 
   const int32_t* topk = a.topk + call_unit * K;
@@ -146,32 +165,28 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   const int32_t step = *a.d_step;
   const int32_t ctx = a.ctx_len[r];
 
-  // ---- 0. load unit state, clear tables ---------------------------------
+  int err = 0;
+  int n_serve = 0;
   if (tid == 0) *s_err = 0;
+  if (crank == 0) {
+  // ---- 0. load unit state, clear tables ---------------------------------
+  int32_t* inv_u = a.inv + (int64_t)l * a.host_tokens + a.host_off[r];
   for (int s = tid; s < B; s += kThreads) {
-    s_slot_pos[s] = g_slot_pos[s];
     s_order[s] = g_order[s];
     s_flag[s] = 0;
   }
-  for (int h = tid; h <= slot_mask; h += kThreads) s_slot_hash[h] = -1;
   for (int h = tid; h <= sel_mask; h += kThreads) {
     s_sel_key[h] = -1;
     s_sel_j[h] = INT32_MAX;
   }
   for (int i = tid; i < hot_per_req; i += kThreads)
     s_hot[i] = a.hot_block[(int64_t)r * hot_per_req + i];
+  const bool ptab_in_smem = a.max_pages <= kMaxSmemPages;
+  if (ptab_in_smem)
+    for (int i = tid; i < a.max_pages; i += kThreads) s_ptab[i] = ptab[i];
   __syncthreads();
 
-  // ---- 1. build the slot hash and the selection hash -------------------
-  for (int s = tid; s < B; s += kThreads) {
-    const int32_t p = s_slot_pos[s];
-    if (p < 0) continue;
-    uint32_t h = hash_pos(p, a.slot_bits);
-    for (int probe = 0; probe <= slot_mask; ++probe) {
-      if (atomicCAS(&s_slot_hash[h], -1, s) == -1) break;
-      h = (h + 1) & slot_mask;
-    }
-  }
+  // ---- 1. build the selection hash ---------------------------------------
   const int j0 = tid * a.kpt;
   int32_t my_p[8];
 #pragma unroll
@@ -193,7 +208,6 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   __syncthreads();
 
   // ---- 2. classify; refresh hits ----------------------------------------
-  int err = 0;
   uint32_t miss_mask = 0;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
         continue;
       }
     }
-    const int32_t blk = ptab[p / P];
+    const int32_t blk = ptab_in_smem ? s_ptab[p / P] : ptab[p / P];
     if (blk >= 0) {  // resident page: read in place, LRU untouched
       if (blk >= a.blocks_per_layer) {
         err |= HS_DEV_ERR_BLOCK;
@@ -236,19 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       out[j] = row;
       continue;
     }
-    int32_t slot = -1;
-    {
-      uint32_t h = hash_pos(p, a.slot_bits);
-      for (int probe = 0; probe <= slot_mask; ++probe) {
-        const int32_t s = s_slot_hash[h];
-        if (s < 0) break;
-        if (s_slot_pos[s] == p) {
-          slot = s;
-          break;
-        }
-        h = (h + 1) & slot_mask;
-      }
-    }
+    const int32_t slot = inv_u[p];  // hot slot holding p, or -1
     if (slot >= 0) {  // hot hit: refresh the LRU entry
       s_flag[slot] = 1;
       g_stamp[slot] = step;
@@ -281,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   }
   int n_cand;
   int rank = block_exclusive_scan(__popc(cand_mask), s_warp, &n_cand);
-  const int n_serve = n_miss_total < n_cand ? n_miss_total : n_cand;
+  n_serve = n_miss_total < n_cand ? n_miss_total : n_cand;
   if (n_miss_total > n_cand) err |= HS_DEV_ERR_CAPACITY;
 #pragma unroll 4
   for (int q = 0; q < 16; ++q) {
@@ -317,6 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     const int j = s_miss_j[i];
     if (i < n_serve) {
       const int32_t s = s_victim[i], p = s_miss_p[i];
+      const int32_t old = g_slot_pos[s];
+      if (old >= 0) inv_u[old] = -1;  // evicted (distinct from every missed position)
+      inv_u[p] = s;
       g_slot_pos[s] = p;
       g_stamp[s] = step;
       out[j] = s_hot[s / P] * P + s % P;
@@ -330,11 +335,33 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     }
   }
 
+  }  // end of CTA 0's metadata work
+
   // ---- 5. copy missed rows: mapped pinned host -> hot slot in HBM --------
-  const int rv = a.row_vec;
+  int* s_nserve = s_warp + kWarps + 1;
+  if (C > 1) {
+    if (crank == 0 && tid == 0) *s_nserve = n_serve;
+    hs_ptx::cluster_sync();  // CTA 0's miss list and hot blocks are complete
+    if (crank != 0) {
+      auto peer = [&](const void* p) { return hs_ptx::mapa(hs_ptx::smem_u32(p), 0); };
+      n_serve = (int)ld_cluster_u32(peer(s_nserve));
+      const int lo = (int)((int64_t)n_serve * crank / C), hi = (int)((int64_t)n_serve * (crank + 1) / C);
+      for (int i = lo + tid; i < hi; i += kThreads) {
+        s_miss_p[i] = (int32_t)ld_cluster_u32(peer(s_miss_p + i));
+        s_victim[i] = (int32_t)ld_cluster_u32(peer(s_victim + i));
+      }
+      for (int i = tid; i < hot_per_req; i += kThreads)
+        s_hot[i] = (int32_t)ld_cluster_u32(peer(s_hot + i));
+    }
+    __syncthreads();
+    hs_ptx::cluster_sync();  // every CTA holds its share: CTA 0 may run ahead and exit
+  }
+  const int i_lo = (int)((int64_t)n_serve * crank / C);
+  const int i_hi = (int)((int64_t)n_serve * (crank + 1) / C);
+  const int rv = RV_CT ? RV_CT : a.row_vec;
   const uint4* hsrc = a.host_pool + ((int64_t)l * a.host_tokens + a.host_off[r]) * rv;
   uint4* kdst = a.kv_pool + (int64_t)l * a.blocks_per_layer * P * rv;
-  const int64_t total = (int64_t)n_serve * rv;
+  const int64_t total = (int64_t)(i_hi - i_lo) * rv;
   for (int64_t base = tid; base < total; base += (int64_t)kThreads * kCopyUnroll) {
     uint4 v[kCopyUnroll];
     int64_t dst[kCopyUnroll];
@@ -343,8 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       const int64_t c = base + (int64_t)u * kThreads;
       dst[u] = -1;
       if (c < total) {
-        const int i = (int)(c / rv);
-        const int e = (int)(c - (int64_t)i * rv);
+        const int ii = (int)(c / rv);
+        const int e = (int)(c - (int64_t)ii * rv);
+        const int i = i_lo + ii;
         const int32_t s = s_victim[i];
         v[u] = __ldcs(hsrc + (int64_t)s_miss_p[i] * rv + e);
         dst[u] = ((int64_t)s_hot[s / P] * P + s % P) * rv + e;
@@ -355,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       if (dst[u] >= 0) kdst[dst[u]] = v[u];
   }
 
-  if (tid == 0 && a.miss_count) a.miss_count[call_unit] = n_serve;
+  if (crank == 0 && tid == 0 && a.miss_count) a.miss_count[call_unit] = n_serve;
   if (err) atomicOr(s_err, err);
   __syncthreads();
   if (tid == 0 && *s_err) atomicOr(a.error_word, *s_err);
@@ -370,16 +398,17 @@ int ceil_log2(int64_t x) {
 }  // namespace
 
 hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes) {
-  const int slot_bits = ceil_log2(2 * (int64_t)B) < 5 ? 5 : ceil_log2(2 * (int64_t)B);
   const int sel_bits = ceil_log2(2 * (int64_t)K) < 5 ? 5 : ceil_log2(2 * (int64_t)K);
-  const size_t smem = smem_plan(K, B, P, slot_bits, sel_bits).total;
+  const size_t smem = smem_plan(K, B, P, sel_bits).total;
   *smem_bytes = smem;
   int dev = 0, optin = 0;
   HS_CUDA_TRY(cudaGetDevice(&dev));
   HS_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
   if (smem > (size_t)optin) return HS_ERR_INVALID;  // K and B too large for one CTA
-  HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem));
+  HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<256, 72>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<0, 0>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   return HS_OK;
 }
 
@@ -399,6 +428,7 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
   a.slot_pos = p->slot_pos;
   a.slot_stamp = p->slot_stamp;
   a.lru_order = p->lru_order;
+  a.inv = p->inv;
   a.host_pool = static_cast<const uint4*>(p->host_pool_dev);
   a.kv_pool = static_cast<uint4*>(p->kv_pool);
   a.error_word = p->error_word;
@@ -411,17 +441,33 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
   a.P = p->d.page_tokens;
   a.max_pages = p->d.max_pages;
   a.row_vec = p->d.row_elems / 8;
-  a.slot_bits = ceil_log2(2 * (int64_t)a.B) < 5 ? 5 : ceil_log2(2 * (int64_t)a.B);
   a.sel_bits = ceil_log2(2 * (int64_t)a.K) < 5 ? 5 : ceil_log2(2 * (int64_t)a.K);
   a.kpt = (a.K + kThreads - 1) / kThreads;
   a.bpt = (a.B + kThreads - 1) / kThreads;
   if (a.kpt > 8 || a.bpt > 16) return HS_ERR_INVALID;
   // The kernel's dynamic shared-memory limit was raised by hs_pool_create
   // (hs_resolve_configure): nothing here may call outside the stream.
-  const size_t smem = smem_plan(a.K, a.B, a.P, a.slot_bits, a.sel_bits).total;
-  dim3 grid(a.R, num_layers);
-  resolve_kernel<<<grid, kThreads, smem, stream>>>(a);
-  HS_CUDA_TRY(cudaGetLastError());
+  const size_t smem = smem_plan(a.K, a.B, a.P, a.sel_bits).total;
+  // copy helpers per unit: enough CTAs to put every SM to work on the copies
+  int C = p->num_sms / (a.R * num_layers);
+  C = C >= 8 ? 8 : C >= 4 ? 4 : C >= 2 ? 2 : 1;
+  a.copy_ctas = C;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.R * C, num_layers);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = C > 1 ? 1 : 0;
+  if (a.P == 256 && a.row_vec == 72)
+    HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<256, 72>, a));
+  else
+    HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<0, 0>, a));
   return HS_OK;
 }
 
