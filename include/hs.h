@@ -69,6 +69,9 @@ typedef enum {
 #define HS_DEV_ERR_BLOCK 8     /* page table / row id names a block outside the pool */
 #define HS_DEV_ERR_WAIT 16     /* an in-kernel bounded wait gave up */
 #define HS_DEV_ERR_INTERNAL 32 /* a kernel found its own launch set-up unusable and did nothing */
+#define HS_DEV_ERR_VALUE 64    /* attention: a value element (first 512 columns of a selected
+                                  row) is not finite or has magnitude >= 65536; the P.V
+                                  product runs in fp16 (see hs_sparse_mla_decode) */
 
 typedef struct {
   int32_t num_requests;    /* R */
@@ -181,6 +184,12 @@ hs_status hs_gather(hs_pool* pool, int32_t layer, const int32_t* row_ids,
  *   out[r][h][e] = sum_j softmax_j(s[h][.]) * kv(row_ids[r][j])[e],  e < v_dim
  * over the j with row_ids >= 0 (v = the first v_dim = 512 columns of each
  * row).  bf16 inputs, fp32 accumulation on the tensor cores, bf16 output.
+ * Scores use bf16 q and rows as given.  The probabilities and the value
+ * columns enter the P.V product as fp16, which holds every bf16 value of
+ * magnitude below 65536 exactly (values below 2^-14 lose low bits, at most
+ * 2^-25 each) and gives the probabilities 11 significant bits; a value
+ * element that is not finite or has magnitude >= 65536 sets error bit VALUE
+ * (that request's output is then not meaningful).
  *   q        device bf16 [R][num_heads][row_elems]   (num_heads <= 128)
  *   row_ids  device int32 [R][K] (e.g. hs_resolve's output for this layer)
  *   out      device bf16 [R][num_heads][v_dim]

@@ -12,22 +12,29 @@
 // Work split.  The fp32 output accumulator O (128 heads x 512) fills a whole
 // SM's tensor memory, so each (request, split-of-K) is handled by a CTA pair
 // (a cluster of 2):
-//   CTA 0 ("score"): Q lives in tensor memory (the A operand); 64-row KV
-//     tiles are gathered by TMA (tile::gather4, 4 rows per instruction, 128B
-//     swizzle); S = Q K^T (M=128, N=64, K=576) goes to a double-buffered TMEM
+//   CTA 0 ("score"): Q lives in tensor memory (the A operand); S = Q K^T
+//     (M=128, N=64, K=576) over 64-row tiles goes to a double-buffered TMEM
 //     accumulator; 4 warps run the online softmax (one thread per head) and
-//     write P as two bf16 parts (hi + lo, so P carries ~16 bits: bf16 P alone
-//     would cost ~1e-3 relative error), which one bulk copy sends into CTA 1.
-//   CTA 1 ("value"): gathers the V part (first 512 columns) of the same rows
-//     the same way and accumulates O += P_hi V + P_lo V (M=128, N=256 x 2, V
-//     as an MN-major operand).  Its 4 epilogue warps rescale O when the
+//     write P in fp16 (11 significant bits; bf16 P would cost ~1.5e-3 relative
+//     error), which one bulk copy sends into CTA 1.
+//   CTA 1 ("value"): accumulates O += P V (M=128, N=256 x 2, V as an MN-major
+//     operand) with V in fp16 as well.  Its 4 epilogue warps rescale O when the
 //     running max moved (lazily: only when it grew by more than 2^8, so the
-//     rescale is rare and off the common path) and write the normalised output.
+//     rescale is rare and off the common path) and write the output through
+//     shared memory in coalesced rows.
+// Row loads.  Each CTA loads the tile rows it needs itself (CTA 0: all 576
+// columns, CTA 1: the 512 value columns), so the two stage rings never wait on
+// each other.  Eleven loader warps per CTA move the rows with 16-byte vector
+// loads into registers and store them into the 128B-swizzled operand layout;
+// a loader thread issues its loads for tile t+1 before it waits for the stage
+// to free up, so the loads overlap the MMAs.  (Plain vector loads move about
+// twice the bytes per SM-clock that TMA row gathers do for scattered 1152-byte
+// rows, and CTA 1 converts its values to fp16 on the way through registers.)
 // Q reaches CTA 0 by TMA (swizzled, then TMEM), each split's row ids are staged
-// in shared memory once, MMA descriptors are computed once and advanced by
-// constants, and every hand-off is an mbarrier.  With several splits per
-// request, each pair writes a normalised fp32 partial and its log-sum-exp; a
-// small merge kernel combines them.
+// in shared memory once by all loader warps, MMA descriptors are computed once
+// and advanced by constants, and every hand-off is an mbarrier.  With several
+// splits per request, each pair writes a normalised fp32 partial and its
+// log-sum-exp; a small merge kernel combines them.
 //
 // Every wait is bounded: a wait that times out sets HS_DEV_ERR_WAIT in the
 // pool's error word and the CTA winds down (no further MMAs), frees its tensor
@@ -35,6 +42,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include <new>
@@ -51,51 +59,72 @@ constexpr int kD = 576;            // row width (latent 512 + rope 64)
 constexpr int kDV = 512;           // value width
 constexpr int kTile = 64;          // KV rows per tile
 constexpr int kStages = 2;         // KV tile ring depth
-constexpr int kThreads = 384;
-constexpr int kLoadWarps = 7;      // warps 1..7 issue the TMA row gathers
-constexpr int kMathWarp0 = 8;      // warps 8..11: softmax (CTA 0) / rescale + epilogue (CTA 1)
+constexpr int kThreads = 512;
+// Warp roles (four warpgroups of four warps):
+//   warp 0       MMA issuer               warp 1 (CTA 0)  rope-block TMA gathers
+//   warps 2..3   idle                     warps 4..11     value-column loaders
+//   warps 12..15 softmax (CTA 0) / rescale + epilogue (CTA 1)
+constexpr int kLoadWarp0 = 4;
+constexpr int kLoadWarps = 8;
+constexpr int kLoadThreads = kLoadWarps * 32;
+static_assert(kLoadThreads == 4 * 64, "loader mapping: 64 value chunks x 4 groups of 16 rows");
+constexpr int kRopeWarp = 1;
+constexpr int kMathWarp0 = 12;
+// Registers per thread after the split (setmaxnreg, per warpgroup).  The kernel
+// launches with 128 per thread (512 threads x 128 = the SM's 65536); the split
+// 72 + 152 + 152 + 136 sums to 4 x 128, so every increase can be granted.
+constexpr int kRegsWG0 = 72, kRegsLoad = 152, kRegsMath = 136;
+static_assert(kRegsWG0 + 2 * kRegsLoad + kRegsMath == 4 * 128, "register split");
 constexpr int kCbK = kD / 64;      // 9 swizzled 128-byte column blocks per K row
-constexpr int kCbV = kDV / 64;     // 8 for V
+constexpr int kChunksK = kD / 8;   // 72 16-byte chunks per K row
 
 constexpr uint32_t kBlockBytes = kTile * 128;              // one column block of a tile: 8192
 constexpr uint32_t kStageBytes = kCbK * kBlockBytes;       // 73728
 constexpr uint32_t kQBlockBytes = kHeads * 128;            // 16384
-constexpr uint32_t kPBytes = kHeads * kTile * 2;           // 16384 per part
-constexpr uint32_t kPMetaBytes = 528;                      // alpha[128] floats + 4 flag words
-constexpr uint32_t kPCopyBytes = 2 * kPBytes + kPMetaBytes;    // 33296 (multiple of 16)
-constexpr uint32_t kPBufBytes = 2 * kPBytes + 1024;        // 33792
+constexpr uint32_t kPBytes = kHeads * kTile * 2;           // 16384 (fp16)
+// P buffer: P [128 heads x 64 rows] fp16, then alpha[128] (fp32), then one
+// 16-byte flag record per softmax warp.  Each softmax warp sends its own 32
+// heads' slice (4096 B of P, 128 B of alpha, its flag record) by bulk copy.
+constexpr int kPBufs = 4;                                  // P ring depth
+constexpr uint32_t kPWarpBytes = kPBytes / 4;              // 4096
+constexpr uint32_t kPAlphaOff = kPBytes;                   // alpha[128]
+constexpr uint32_t kPFlagOff = kPBytes + 512;              // 4 x 16-byte flag records
+constexpr uint32_t kPCopyBytes = 4 * (kPWarpBytes + 128 + 16);  // 16960 per tile
+constexpr uint32_t kPBufBytes = kPBytes + 1024;            // 17408
 
-// Shared-memory layout, identical offsets in both CTAs of a pair (the bulk
-// copy and remote barrier operations address the peer by offset).  Swizzled
-// regions are 1024-byte aligned.
+// Shared-memory layout.  The P buffers, m/l and the barriers sit at the same
+// offsets in both CTAs of a pair (the bulk copy and remote barrier operations
+// address the peer by offset).  Swizzled regions are 1024-byte aligned.
 constexpr int kMaxSplitRows = 2048;  // row ids of one split, staged in shared memory
 constexpr uint32_t OFF_STAGE = 0;    // CTA 0 first holds Q here (9 x 16384 B)
 constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // 147456
-constexpr uint32_t OFF_ML = OFF_P + 2 * kPBufBytes;            // 215040: m[128], l[128]
-constexpr uint32_t OFF_RID = OFF_ML + 1024;                    // 216064: int32 [2048]
-constexpr uint32_t OFF_BAR = OFF_RID + 4 * kMaxSplitRows;      // 224256
+constexpr uint32_t OFF_ML = OFF_P + kPBufs * kPBufBytes;       // 217088: m[128], l[128]
+constexpr uint32_t OFF_RID = OFF_ML + 1024;                    // 218112: int32 [2048]
+constexpr uint32_t OFF_BAR = OFF_RID + 4 * kMaxSplitRows;      // 226304
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
-constexpr uint32_t kSmemBytes = OFF_MISC + 64;                 // 224576
+constexpr uint32_t kSmemBytes = OFF_MISC + 64;                 // 226624
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 static_assert(kCbK * kQBlockBytes <= kStages * kStageBytes, "Q must fit the stage region");
+// epilogue staging (4 warps x 8 KiB) reuses the stage region once the last tile is consumed
+static_assert(4 * 8192 <= kStages * kStageBytes, "epilogue staging");
 
 // barrier indices (8 bytes each at OFF_BAR)
 enum {
-  B_KV_FULL = 0,     // [2] TMA complete_tx -> MMA (both CTAs: K tile / V tile)
+  B_KV_FULL = 0,     // [2] loader warps stored a tile -> MMA (both CTAs: K tile / V tile)
   B_KV_EMPTY = 2,    // [2] MMA commit -> loaders
   B_S_FULL = 4,      // [2] score MMA commit -> softmax
   B_S_EMPTY = 6,     // [2] softmax -> score MMA
-  B_P_EMPTY = 8,     // [2] (CTA 0) value MMA commit (multicast) -> softmax
-  B_Q_SMEM = 10,     // (CTA 0) TMA of Q landed in shared memory
-  B_Q_READY = 11,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loader
-  B_P_FULL = 12,     // [2] (CTA 1) bulk copy complete_tx -> value MMA
-  B_RID = 14,        // loader warp staged this split's row ids
-  B_CORR_REQ = 15,   // (CTA 1) value MMA -> rescale warps
-  B_CORR_DONE = 16,  // (CTA 1) rescale warps -> value MMA
-  B_MMA_IDLE = 17,   // (CTA 1) commit: earlier P.V MMAs finished
-  B_ML_FULL = 18,    // (CTA 1) softmax's final m, l -> epilogue
-  B_FINAL = 19,      // MMA issuer's last commit
-  B_P_READY = 20,    // [2] (CTA 0) softmax threads wrote P -> bulk-copy issuer
-  B_COUNT = 22
+  B_P_EMPTY = 8,     // [4] (CTA 0) value MMA commit (multicast) -> softmax
+  B_P_FULL = 12,     // [4] (CTA 1) bulk copies complete_tx -> value MMA
+  B_Q_SMEM = 16,     // (CTA 0) TMA of Q landed in shared memory
+  B_Q_READY = 17,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loaders
+  B_RID = 18,        // loader warps staged this split's row ids
+  B_CORR_REQ = 19,   // (CTA 1) value MMA -> rescale warps
+  B_CORR_DONE = 20,  // (CTA 1) rescale warps -> value MMA
+  B_MMA_IDLE = 21,   // (CTA 1) commit: earlier P.V MMAs finished
+  B_ML_FULL = 22,    // (CTA 1) softmax's final m, l -> epilogue
+  B_FINAL = 23,      // MMA issuer's last commit
+  B_COUNT = 24
 };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 
@@ -105,18 +134,21 @@ constexpr uint32_t TM_S = 288;   // CTA 0: S, 2 x 64 columns
 constexpr uint32_t TM_O = 0;     // CTA 1: O, 512 columns
 
 constexpr uint32_t kIdescS = idesc_bf16(128, kTile, false, false);  // A (TMEM), B K-major
-constexpr uint32_t kIdescPV = idesc_bf16(128, 256, false, true);    // A K-major, B MN-major
+// kind::f16 with fp16 A and B (format code 0), fp32 D; A K-major, B MN-major
+constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((uint32_t)(256 >> 3) << 17) |
+                              ((uint32_t)(128 >> 4) << 24);
 
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before giving up
 
 struct AttnArgs {
+  const uint4* kv;          // this layer's rows, [rows_in_layer][576] bf16 as 16-byte chunks
   const int32_t* row_ids;   // [R][K]
   uint16_t* out;            // [R][H][512] bf16 (splits == 1)
   float* lse;               // [R][H] or null (splits == 1)
   float* ws_o;              // [R][splits][128][512] (splits > 1)
   float* ws_lse;            // [R][splits][128]
   int32_t* error_word;
-  int32_t rows_in_layer;    // also the out-of-range row coordinate (TMA fills zeros)
+  int32_t rows_in_layer;
   int32_t K, H, splits, rows_per_split;
   float scale_log2;         // scale * log2(e)
 };
@@ -134,7 +166,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   if (*abort) return false;
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
-    const bool ok = cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    const bool ok = cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
     if (ok) return true;
     if ((i & 63) == 63) {
       if (*abort) return false;
@@ -150,10 +182,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-// Same, for roles run by whole warps: every lane gets the same answer, so
-// warp-collective tcgen05 instructions after it are executed uniformly.
+// Same, for roles run by whole warps: lane 0 polls (one poller per warp keeps
+// the barrier traffic off the shared-memory pipe the MMAs read operands
+// through), then the warp synchronises, which orders lane 0's acquire before
+// every lane's later accesses; every lane gets the same answer, so
+// warp-collective instructions after it are executed uniformly.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort,
                                               int32_t* error_word, bool cluster_scope = false) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, error_word, cluster_scope);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
+// Same, with every lane polling: for the MMA warp, whose tcgen05 issue
+// (elect.sync) wants the warp converged at all times.
+__device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             int32_t* error_word, bool cluster_scope = false) {
   const bool ok = wait_bar(bar, parity, abort, error_word, cluster_scope);
   return __all_sync(0xffffffffu, ok);
 }
@@ -168,6 +214,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Two bf16 values (one 32-bit word) -> the same two values as fp16, exact for
+// magnitudes in [2^-14, 65536).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 // Shared-memory descriptor of a 128B-swizzled operand (atoms of 8 rows x 128 B).
@@ -185,18 +241,14 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
       : "memory");
 }
-// (unused: both CTAs gather their own rows, see the loader role)
-// Same 4 rows, delivered to the same shared-memory offset (and completing
-// bytes on the same barrier offset) in every CTA of cta_mask.
-__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const CUtensorMap* map, int x, int y0,
-                                               int y1, int y2, int y3, uint32_t bar,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar),
-      "h"(cta_mask)
-      : "memory");
+// Register budget of this warpgroup from here on (all its warps execute it).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 // TMA: one box (64 columns x box rows) from (x, y) into dst.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -206,6 +258,136 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// 16-byte global load through the read-only path, not kept in L1 (each row is
+// read once per CTA; the pair's second read of it hits L2).
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+// Same, at row_base + row * 1152 bytes (one KV row), row >= 0; the address is
+// formed inside the statement so it occupies no register beyond the load.
+__device__ __forceinline__ uint4 ld_row_chunk(const uint4* row_base, int row) {
+  uint4 v;
+  asm volatile(
+      "{\n .reg .u64 a;\n mad.wide.s32 a, %4, 1152, %5;\n"
+      " ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [a];\n}"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "r"(row), "l"(row_base));
+  return v;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+// per-halfword unsigned max
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Value-column loaders: move the first 512 columns of the tile rows into the
+// stage ring, 16-byte chunks in the 128B-swizzled K-major layout the MMAs read
+// (column block c/8 at +8192 each, row at +128, chunk c%8 at position
+// (c%8) ^ (row%8)).  Loader thread lt owns chunk c = lt % 64 of rows
+// 16*(lt/64) .. +15 of every tile, so its shared-memory offsets are fixed and
+// its row ids come in 16-byte reads.  A thread issues its loads for tile t+1
+// before it waits for that tile's stage to free up.
+// TO_F16 converts the values to fp16 on the way.  A row id of -1 stores zeros.
+struct ValueLoader {
+  const uint4* col;  // chunk c of row 0
+  const int32_t* s_rid;
+  uint32_t stage0, soff, c7s;
+  int r0;
+
+  __device__ __forceinline__ ValueLoader(const uint4* kv, const int32_t* s_rid_, uint32_t stage0_,
+                                         int lt)
+      : s_rid(s_rid_), stage0(stage0_) {
+    r0 = (lt >> 6) * 16;
+    const int c = lt & 63;
+    col = kv + c;
+    soff = (uint32_t)((c >> 3) * kBlockBytes + r0 * 128);
+    c7s = (uint32_t)(c & 7) << 4;
+  }
+  __device__ __forceinline__ void issue(int t, uint4 (&v)[16]) const {
+    const int32_t* rid = s_rid + t * kTile + r0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int4 w = *reinterpret_cast<const int4*>(rid + 4 * i);
+      const int32_t ids[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        v[4 * i + j] = ids[j] >= 0 ? ld_row_chunk(col, ids[j]) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  template <bool TO_F16>
+  __device__ __forceinline__ void store(int t, uint4 (&v)[16], uint32_t& vmax) const {
+    const uint32_t stage = stage0 + (uint32_t)(t % kStages) * kStageBytes;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      uint4 x = v[k];
+      if (TO_F16) {
+        vmax = max_u16x2(vmax, x.x & 0x7fff7fffu);
+        vmax = max_u16x2(vmax, x.y & 0x7fff7fffu);
+        vmax = max_u16x2(vmax, x.z & 0x7fff7fffu);
+        vmax = max_u16x2(vmax, x.w & 0x7fff7fffu);
+        x.x = bf16x2_to_f16x2(x.x);
+        x.y = bf16x2_to_f16x2(x.y);
+        x.z = bf16x2_to_f16x2(x.z);
+        x.w = bf16x2_to_f16x2(x.w);
+      }
+      // row r0 + k: r0 % 8 == 0, so its swizzle phase is k % 8
+      st_shared_v4(stage + soff + (uint32_t)k * 128u + (c7s ^ ((uint32_t)(k & 7) << 4)), x);
+    }
+  }
+};
+
+// The loader warps' loop.  The first store waits for q_ready_bar if it is
+// non-zero (Q occupies the stage region until it has moved to TMEM).  Returns
+// error bits.
+template <bool TO_F16>
+__device__ __forceinline__ int load_values(const ValueLoader& L, int n_tiles, uint32_t bar_full0,
+                                           uint32_t bar_empty0, uint32_t q_ready_bar,
+                                           volatile int* abort_flag, int32_t* error_word) {
+  uint32_t vmax = 0;  // per-halfword max of |bf16| bit patterns seen (TO_F16)
+  bool need_q = q_ready_bar != 0;
+  const int lane = threadIdx.x & 31;
+  auto put = [&](int t, uint4 (&v)[16]) -> bool {
+    if (need_q) {
+      if (!wait_bar_warp(q_ready_bar, 0, abort_flag, error_word)) return false;
+      need_q = false;
+    }
+    const int s = t % kStages;
+    if (!wait_bar_warp(bar_empty0 + 8u * s, ((uint32_t)(t / kStages) & 1u) ^ 1u, abort_flag,
+                       error_word))
+      return false;
+    L.store<TO_F16>(t, v, vmax);
+    fence_proxy_async_smem();  // generic-proxy stores -> visible to the MMA
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_full0 + 8u * s);
+    return true;
+  };
+  uint4 va[16];
+  for (int t = 0; t < n_tiles; ++t) {
+    L.issue(t, va);
+    if (!put(t, va)) break;
+  }
+  // 0x4780 is bf16 65536: from there up (inf and NaN included) fp16 cannot hold it
+  if (TO_F16 && ((vmax & 0xffffu) >= 0x4780u || (vmax >> 16) >= 0x4780u)) return HS_DEV_ERR_VALUE;
+  return 0;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -233,17 +415,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- set-up: barriers, tensor memory ---------------------------------
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_KV_FULL + i), 1);
+      // loader warps (+ the rope-gather arm in CTA 0)
+      mbar_init(bar(B_KV_FULL + i), kLoadWarps + (rank == 0 ? 1 : 0));
       mbar_init(bar(B_KV_EMPTY + i), 1);
       mbar_init(bar(B_S_FULL + i), 1);
       mbar_init(bar(B_S_EMPTY + i), 128);
+    }
+    for (int i = 0; i < kPBufs; ++i) {
       mbar_init(bar(B_P_EMPTY + i), 1);
       mbar_init(bar(B_P_FULL + i), 1);
-      mbar_init(bar(B_P_READY + i), 128);
     }
     mbar_init(bar(B_Q_SMEM), 1);
     mbar_init(bar(B_Q_READY), 128);
-    mbar_init(bar(B_RID), 32);
+    mbar_init(bar(B_RID), kLoadWarps);
     mbar_init(bar(B_CORR_REQ), 1);
     mbar_init(bar(B_CORR_DONE), 128);
     mbar_init(bar(B_MMA_IDLE), 1);
@@ -267,133 +451,171 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tm = *tmem_holder;
   int err = 0;
 
-  if (warp >= 1 && warp <= kLoadWarps) {
-    // ================= loader warps (both CTAs): TMA issue =================
-    // Each CTA gathers its own copy of the rows (CTA 0: all 9 column blocks,
-    // CTA 1: the 8 value blocks), so a stage is released by that CTA's MMA
-    // alone.  The row gathers are spread over 7 warps: TMA issue throughput
-    // grows with the number of issuing warps.
-    const int lw = warp - 1;
-    if (rank == 0 && lw == 0 && lane == 0 && !*abort_flag) {  // Q[r] (128 rows) -> smem
+  // Common exit: report errors, free tensor memory once every role is done, and
+  // keep the CTA alive until its peer no longer addresses it.  Each role runs
+  // it at its own end (the roles run under different register budgets, so
+  // their code paths do not join again).
+  auto finish = [&]() {
+    if (err) atomicOr(a.error_word, err);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tm, 512);
+    cluster_sync();
+  };
+
+  // Each role first sets its warpgroup's register budget (kRegsWG0 ...); the
+  // four warps of a warpgroup always take the same budget.
+  if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoadWarps) {
+    // ================= value-column loaders (both CTAs) =================
+    const int lt = tid - kLoadWarp0 * 32;
+    {  // this split's row ids -> shared memory, validated once (-1 = no row)
+      constexpr int kRidPer = (kMaxSplitRows + kLoadThreads - 1) / kLoadThreads;
+      const int32_t* g_rows = a.row_ids + (int64_t)r * a.K;
+      const int n_rows = n_tiles * kTile;
+      int32_t v[kRidPer];
+#pragma unroll
+      for (int k = 0; k < kRidPer; ++k) {
+        const int i = lt + k * kLoadThreads, j = j_begin + i;
+        v[k] = (i < n_rows && j < j_end) ? __ldg(g_rows + j) : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < kRidPer; ++k) {
+        const int i = lt + k * kLoadThreads;
+        if (i < n_rows) {
+          int32_t x = v[k];
+          if (x < -1 || x >= a.rows_in_layer) {
+            err |= HS_DEV_ERR_BLOCK;
+            x = -1;
+          }
+          s_rid[i] = x;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_RID));
+    }
+    if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word)) {
+      const ValueLoader L(a.kv, s_rid, sbase + OFF_STAGE, lt);
+      if (rank == 0)
+        err |= load_values<false>(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), bar(B_Q_READY),
+                                  abort_flag, a.error_word);
+      else
+        err |= load_values<true>(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
+                                 a.error_word);
+    }
+    finish();
+    return;
+  } else if (warp == kRopeWarp && rank == 0) {
+    // ================= Q load, then the rope column block (CTA 0) =================
+    if (lane == 0 && !*abort_flag) {  // Q[r] (128 rows) -> smem by TMA
       mbar_arrive_expect_tx(bar(B_Q_SMEM), kCbK * kQBlockBytes);
       for (int cb = 0; cb < kCbK; ++cb)
         tma_load_2d(sbase + OFF_STAGE + cb * kQBlockBytes, &q_map, cb * 64, r * a.H,
                     bar(B_Q_SMEM));
     }
-    if (lw == 0) {  // this split's row ids -> shared memory, validated once (-1 = no row)
-      const int32_t* g_rows = a.row_ids + (int64_t)r * a.K;
-      for (int i = lane; i < n_tiles * kTile; i += 32) {
-        const int j = j_begin + i;
-        int32_t v = j < j_end ? __ldg(g_rows + j) : -1;
-        if (v < -1 || v >= a.rows_in_layer) {
-          err |= HS_DEV_ERR_BLOCK;
-          v = -1;
+    // rope block (columns 512..575) of each tile: 16 gathers of 4 rows, one per
+    // lane 0..15; a row id of -1 reads past the tensor, which fills zeros
+    if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word) &&
+        wait_bar_warp(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kStages;
+        if (!wait_bar_warp(bar(B_KV_EMPTY + s), ((uint32_t)(t / kStages) & 1u) ^ 1u, abort_flag,
+                           a.error_word))
+          break;
+        if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), kBlockBytes);
+        __syncwarp();
+        if (lane < kTile / 4) {
+          const int32_t* rid = s_rid + t * kTile + 4 * lane;
+          const int y0 = rid[0] >= 0 ? rid[0] : a.rows_in_layer;
+          const int y1 = rid[1] >= 0 ? rid[1] : a.rows_in_layer;
+          const int y2 = rid[2] >= 0 ? rid[2] : a.rows_in_layer;
+          const int y3 = rid[3] >= 0 ? rid[3] : a.rows_in_layer;
+          tma_gather4(sbase + OFF_STAGE + s * kStageBytes + 8 * kBlockBytes + lane * 512, &kv_map,
+                      kDV, y0, y1, y2, y3, bar(B_KV_FULL + s));
         }
-        s_rid[i] = v;
-      }
-      __syncwarp();
-      mbar_arrive(bar(B_RID));
-    }
-    bool ok = wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word);
-    // CTA 0: Q occupies the stage region until it has moved to TMEM
-    if (rank == 0) ok = ok && wait_bar_warp(bar(B_Q_READY), 0, abort_flag, a.error_word);
-    const int ncb = rank == 0 ? kCbK : kCbV;
-    const int n_items = ncb * (kTile / 4);  // (column block, 4-row group) pairs
-    for (int t = 0; ok && t < n_tiles; ++t) {
-      const int s = t % kStages;
-      const uint32_t ph = (uint32_t)(t / kStages) & 1u;
-      if (!wait_bar_warp(bar(B_KV_EMPTY + s), ph ^ 1u, abort_flag, a.error_word)) break;
-      if (lw == 0 && lane == 0)
-        mbar_arrive_expect_tx(bar(B_KV_FULL + s), (uint32_t)ncb * kBlockBytes);
-      if (lane < kTile / 4) {
-        const int32_t* rid = s_rid + t * kTile + 4 * lane;  // lane g moves rows 4g .. 4g+3
-        const int y0 = rid[0] >= 0 ? rid[0] : a.rows_in_layer;
-        const int y1 = rid[1] >= 0 ? rid[1] : a.rows_in_layer;
-        const int y2 = rid[2] >= 0 ? rid[2] : a.rows_in_layer;
-        const int y3 = rid[3] >= 0 ? rid[3] : a.rows_in_layer;
-        const uint32_t dst = sbase + OFF_STAGE + s * kStageBytes + lane * 512;
-        for (int item = lw * 16 + lane; item < n_items; item += kLoadWarps * 16) {
-          const int cb = item >> 4;
-          tma_gather4(dst + cb * kBlockBytes, &kv_map, cb * 64, y0, y1, y2, y3, bar(B_KV_FULL + s));
-        }
+        __syncwarp();
       }
     }
+    finish();
+    return;
   } else if (warp == 0) {
-    // ================= MMA issuer =================
-    if (lane == 0) {
-      if (rank == 0) {
-        // B = K tile, K-major, 128B swizzle: column block cb at +cb*8192, K step
-        // kk at +(kk%4)*32 inside the block; 8-row groups 1024 B apart
-        const uint64_t kdesc0 = desc_sw128(sbase + OFF_STAGE, 16, 1024);
-        if (wait_bar(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
-          tc_fence_after();
-          for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % kStages, b = t & 1;
-            const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t >> 1) & 1u;
-            if (!wait_bar(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
-            if (!wait_bar(bar(B_S_EMPTY + b), pb ^ 1u, abort_flag, a.error_word)) break;
-            tc_fence_after();
-            const uint64_t kd = kdesc0 + ((s * kStageBytes) >> 4);
-            const uint32_t dS = tm + TM_S + b * kTile;
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-              mma_ts(dS, tm + TM_Q + kk * 8,
-                     kd + (uint64_t)((((kk >> 2) * kBlockBytes) + (kk & 3) * 32) >> 4), kIdescS,
-                     kk > 0);
-            mma_commit(bar(B_KV_EMPTY + s));
-            mma_commit(bar(B_S_FULL + b));
-          }
-        }
-      } else {
-        // A = P (interleaved core matrices: K step kk at +kk*256, 8-head groups
-        // 1024 B apart); B = V, MN-major, 128B swizzle: 64-column blocks
-        // 8192 B apart, 8-row groups 1024 B apart, K step kk at +kk*2048
-        const uint64_t pdesc0 = smem_desc(sbase + OFF_P, 128, 1024);
-        const uint64_t vdesc0 = desc_sw128(sbase + OFF_STAGE, kBlockBytes, 1024);
-        uint32_t corr = 0;
+    // ================= MMA issuer (the whole warp runs it; one elected lane issues) =================
+    if (rank == 0) {
+      // B = K tile, K-major, 128B swizzle: column block cb at +cb*8192, K step
+      // kk at +(kk%4)*32 inside the block; 8-row groups 1024 B apart
+      const uint64_t kdesc0 = desc_sw128(sbase + OFF_STAGE, 16, 1024);
+      if (wait_bar_all(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
+        tc_fence_after();
         for (int t = 0; t < n_tiles; ++t) {
           const int s = t % kStages, b = t & 1;
           const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t >> 1) & 1u;
-          mbar_arrive_expect_tx(bar(B_P_FULL + b), kPCopyBytes);
-          if (!wait_bar(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
-          if (!wait_bar(bar(B_P_FULL + b), pb, abort_flag, a.error_word, true)) break;
-          const uint32_t* flags =
-              reinterpret_cast<const uint32_t*>(smem + OFF_P + b * kPBufBytes + 2 * kPBytes + 512);
-          if (t > 0 && (flags[0] | flags[1] | flags[2] | flags[3])) {
-            // the running max moved for some head: rescale O before adding tile t
-            mma_commit(bar(B_MMA_IDLE));
-            if (!wait_bar(bar(B_MMA_IDLE), corr & 1u, abort_flag, a.error_word)) break;
+          if (!wait_bar_all(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
+          if (!wait_bar_all(bar(B_S_EMPTY + b), pb ^ 1u, abort_flag, a.error_word)) break;
+          tc_fence_after();
+          const uint64_t kd = kdesc0 + ((s * kStageBytes) >> 4);
+          const uint32_t dS = tm + TM_S + b * kTile;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ts_elect(dS, tm + TM_Q + kk * 8,
+                         kd + (uint64_t)((((kk >> 2) * kBlockBytes) + (kk & 3) * 32) >> 4),
+                         kIdescS, kk > 0);
+          mma_commit_elect(bar(B_KV_EMPTY + s));
+          mma_commit_elect(bar(B_S_FULL + b));
+        }
+      }
+    } else {
+      // A = P, fp16 (interleaved core matrices: K step kk at +kk*256, 8-head
+      // groups 1024 B apart); B = V, fp16, MN-major, 128B swizzle: 64-column
+      // blocks 8192 B apart, 8-row groups 1024 B apart, K step kk at +kk*2048
+      const uint64_t pdesc0 = smem_desc(sbase + OFF_P, 128, 1024);
+      const uint64_t vdesc0 = desc_sw128(sbase + OFF_STAGE, kBlockBytes, 1024);
+      uint32_t corr = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kStages, b = t % kPBufs;
+        const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t / kPBufs) & 1u;
+        if (lane == 0) mbar_arrive_expect_tx(bar(B_P_FULL + b), kPCopyBytes);
+        __syncwarp();
+        if (!wait_bar_all(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
+        if (!wait_bar_all(bar(B_P_FULL + b), pb, abort_flag, a.error_word, true)) break;
+        const uint32_t* flags =
+            reinterpret_cast<const uint32_t*>(smem + OFF_P + b * kPBufBytes + kPFlagOff);
+        if (t > 0 && (flags[0] | flags[4] | flags[8] | flags[12])) {
+          // the running max moved for some head: rescale O before adding tile t
+          mma_commit_elect(bar(B_MMA_IDLE));
+          if (!wait_bar_all(bar(B_MMA_IDLE), corr & 1u, abort_flag, a.error_word)) break;
+          if (lane == 0) {
             *corr_tile = t;
             mbar_arrive(bar(B_CORR_REQ));
-            if (!wait_bar(bar(B_CORR_DONE), corr & 1u, abort_flag, a.error_word)) break;
-            ++corr;
           }
-          tc_fence_after();
-          const uint64_t pd = pdesc0 + ((b * kPBufBytes) >> 4);
-          const uint64_t vd = vdesc0 + ((s * kStageBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-              for (int half = 0; half < 2; ++half)
-                mma_ss(tm + TM_O + half * 256, pd + (uint64_t)((part * kPBytes + kk * 256) >> 4),
-                       vd + (uint64_t)((half * 4 * kBlockBytes + kk * 2048) >> 4), kIdescPV,
-                       (t > 0 || kk > 0 || part > 0) ? 1u : 0u);
-            }
-          }
-          mma_commit(bar(B_KV_EMPTY + s));
-          mma_commit_multicast(bar(B_P_EMPTY + b), (uint16_t)0x1);  // P buffer b free (CTA 0)
+          if (!wait_bar_all(bar(B_CORR_DONE), corr & 1u, abort_flag, a.error_word)) break;
+          ++corr;
         }
+        tc_fence_after();
+        const uint64_t pd = pdesc0 + ((b * kPBufBytes) >> 4);
+        const uint64_t vd = vdesc0 + ((s * kStageBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+            mma_ss_elect(tm + TM_O + half * 256, pd + (uint64_t)((kk * 256) >> 4),
+                         vd + (uint64_t)((half * 4 * kBlockBytes + kk * 2048) >> 4), kIdescPV,
+                         (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit_elect(bar(B_KV_EMPTY + s));
+        mma_commit_multicast_elect(bar(B_P_EMPTY + b), (uint16_t)0x1);  // P buffer b free (CTA 0)
+      }
+      if (lane == 0) {
         *corr_exit = 1;
         mbar_arrive(bar(B_CORR_REQ));  // releases the rescale warps
       }
-      mma_commit(bar(B_FINAL));
-      wait_bar(bar(B_FINAL), 0, abort_flag, a.error_word);
+      __syncwarp();
     }
-    __syncwarp();
+    mma_commit_elect(bar(B_FINAL));
+    wait_bar_all(bar(B_FINAL), 0, abort_flag, a.error_word);
+    finish();
+    return;
   } else if (warp >= kMathWarp0 && rank == 0) {
-    // ================= softmax (CTA 0, warps 4..7, one thread per head) =================
+    // ================= softmax (CTA 0, warps 12..15, one thread per head) =================
     const int h = tid - kMathWarp0 * 32;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = wait_bar_warp(bar(B_Q_SMEM), 0, abort_flag, a.error_word);
@@ -423,32 +645,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ok = ok && wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word);
     const uint32_t peer_p = mapa(sbase + OFF_P, 1);
     const uint32_t peer_pfull = mapa(bar(B_P_FULL), 1);
+    const int wq = warp & 3;  // this warp's heads: 32 wq .. 32 wq + 31
     float m_used = -INFINITY, l_sum = 0.f;
     for (int t = 0; ok && t < n_tiles; ++t) {
-      const int b = t & 1;
+      const int b = t & 1;  // S buffer
       const uint32_t pb = (uint32_t)(t >> 1) & 1u;
+      const int pbuf_i = t % kPBufs;  // P buffer
+      const uint32_t ppar = (uint32_t)(t / kPBufs) & 1u;
       const uint64_t valid =
           (uint64_t)__ballot_sync(0xffffffffu, s_rid[t * kTile + lane] >= 0) |
           ((uint64_t)__ballot_sync(0xffffffffu, s_rid[t * kTile + lane + 32] >= 0) << 32);
       if (!wait_bar_warp(bar(B_S_FULL + b), pb, abort_flag, a.error_word)) break;
       tc_fence_after();
       float x[kTile];
+      {
+        uint32_t u[kTile];
+        const uint32_t sa = tm + lane_off + TM_S + b * kTile;
 #pragma unroll
-      for (int c = 0; c < kTile; c += 16) {
-        uint32_t u[16];
-        tmem_ld16(tm + lane_off + TM_S + b * kTile + c, u);
+        for (int i = 0; i < 4; ++i) tmem_ld16p(sa + 16 * i, u + 16 * i);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[c + i] = __uint_as_float(u[i]);
+        for (int i = 0; i < kTile; ++i) x[i] = __uint_as_float(u[i]);
       }
       tc_fence_before();
       mbar_arrive(bar(B_S_EMPTY + b));
+      // max of the raw scores (scale > 0 keeps the order); rows without a valid
+      // id become -inf, which the exponent below turns into 0
       float tmax = -INFINITY;
+      if (valid == ~0ull) {
 #pragma unroll
-      for (int i = 0; i < kTile; ++i) {
-        x[i] = ((valid >> i) & 1) ? x[i] * a.scale_log2 : -INFINITY;
-        tmax = fmaxf(tmax, x[i]);
+        for (int i = 0; i < kTile; ++i) tmax = fmaxf(tmax, x[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kTile; ++i) {
+          x[i] = ((valid >> i) & 1) ? x[i] : -INFINITY;
+          tmax = fmaxf(tmax, x[i]);
+        }
       }
+      tmax *= a.scale_log2;
       // lazy rescale: move the reference max only when it grew by > 2^8
       const bool rescale = tmax > m_used + 8.f;
       float alpha = 1.f;
@@ -457,38 +691,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         l_sum *= alpha;
         m_used = tmax;
       }
-      // P buffer b is free once the value CTA finished tile t-2
-      if (!wait_bar_warp(bar(B_P_EMPTY + b), pb ^ 1u, abort_flag, a.error_word)) break;
-      unsigned char* pbuf = smem + OFF_P + b * kPBufBytes;
+      // P buffer t % kPBufs is free once the value CTA finished tile t - kPBufs
+      if (!wait_bar_warp(bar(B_P_EMPTY + pbuf_i), ppar ^ 1u, abort_flag, a.error_word)) break;
+      unsigned char* pbuf = smem + OFF_P + pbuf_i * kPBufBytes;
+      // p = 2^(scale_log2 * x - m_used).  m_used is -inf only while no valid row
+      // has been seen, and then every x is -inf too: adding -inf keeps p = 0.
+      const float neg_m = m_used == -INFINITY ? -INFINITY : -m_used;
 #pragma unroll
       for (int kb = 0; kb < kTile / 8; ++kb) {
-        uint32_t hi[4], lo[4];
+        uint32_t pk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float x0 = x[kb * 8 + 2 * i], x1 = x[kb * 8 + 2 * i + 1];
-          const float p0 = x0 == -INFINITY ? 0.f : fast_exp2(x0 - m_used);
-          const float p1 = x1 == -INFINITY ? 0.f : fast_exp2(x1 - m_used);
+          const float p0 = fast_exp2(fmaf(x[kb * 8 + 2 * i], a.scale_log2, neg_m));
+          const float p1 = fast_exp2(fmaf(x[kb * 8 + 2 * i + 1], a.scale_log2, neg_m));
           l_sum += p0 + p1;
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-          const float2 hf = __bfloat1622float2(h2);
-          hi[i] = *reinterpret_cast<const uint32_t*>(&h2);
-          lo[i] = pack_bf16x2(p0 - hf.x, p1 - hf.y);
+          pk[i] = pack_f16x2(p0, p1);
         }
         // P [128 heads x 64 rows], K-major core matrices (head group, row group)
         const uint32_t off = (uint32_t)(((h >> 3) * (kTile / 8) + kb) * 128 + (h & 7) * 16);
-        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(pbuf + kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      float* meta = reinterpret_cast<float*>(pbuf + 2 * kPBytes);
-      meta[h] = alpha;
+      reinterpret_cast<float*>(pbuf + kPAlphaOff)[h] = alpha;
       const uint32_t any = __ballot_sync(0xffffffffu, rescale && t > 0);
-      if (lane == 0) reinterpret_cast<uint32_t*>(meta + 128)[warp & 3] = any;
-      fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk copy
-      mbar_arrive(bar(B_P_READY + b));
-      if (h == 0) {
-        if (!wait_bar(bar(B_P_READY + b), pb, abort_flag, a.error_word)) break;
-        bulk_copy_s2cluster(peer_p + b * kPBufBytes, sbase + OFF_P + b * kPBufBytes, kPCopyBytes,
-                            peer_pfull + 8u * b);
+      if (lane == 0) reinterpret_cast<uint32_t*>(pbuf + kPFlagOff + 16 * wq)[0] = any;
+      fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk copies
+      __syncwarp();
+      if (lane == 0) {  // this warp's slice -> the value CTA
+        const uint32_t src = sbase + OFF_P + pbuf_i * kPBufBytes;
+        const uint32_t dst = peer_p + pbuf_i * kPBufBytes;
+        const uint32_t fb = peer_pfull + 8u * pbuf_i;
+        bulk_copy_s2cluster(dst + wq * kPWarpBytes, src + wq * kPWarpBytes, kPWarpBytes, fb);
+        bulk_copy_s2cluster(dst + kPAlphaOff + wq * 128, src + kPAlphaOff + wq * 128, 128, fb);
+        bulk_copy_s2cluster(dst + kPFlagOff + wq * 16, src + kPFlagOff + wq * 16, 16, fb);
       }
     }
     // final m, l for this head -> value CTA
@@ -496,36 +730,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     st_cluster_f32(mapa(sbase + OFF_ML + 512 + 4 * h, 1), l_sum);
     mbar_arrive_remote(mapa(bar(B_ML_FULL), 1));
     // wait until the value CTA released the last P buffers (its commits landed)
-    for (int t = n_tiles - 2; t < n_tiles; ++t) {
+    for (int t = n_tiles - kPBufs; t < n_tiles; ++t) {
       if (t < 0) continue;
-      wait_bar(bar(B_P_EMPTY + (t & 1)), (uint32_t)(t >> 1) & 1u, abort_flag, a.error_word);
+      wait_bar_warp(bar(B_P_EMPTY + t % kPBufs), (uint32_t)(t / kPBufs) & 1u, abort_flag,
+                    a.error_word);
     }
+    finish();
+    return;
   } else if (warp >= kMathWarp0) {
-    // ================= rescale + epilogue (CTA 1, warps 4..7) =================
-    const int h = tid - kMathWarp0 * 32;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    // ================= rescale + epilogue (CTA 1, warps 12..15) =================
+    const int h = tid - kMathWarp0 * 32;  // head = TMEM lane
+    const int wq = warp & 3;              // this warp's TMEM lane quarter (heads 32wq ..)
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     for (uint32_t k = 0;; ++k) {  // rare: only tiles where some head's max moved
       if (!wait_bar_warp(bar(B_CORR_REQ), k & 1u, abort_flag, a.error_word)) break;
       if (*corr_exit) break;
       tc_fence_after();
       const int t = *corr_tile;
       const float alpha =
-          reinterpret_cast<const float*>(smem + OFF_P + (t & 1) * kPBufBytes + 2 * kPBytes)[h];
+          reinterpret_cast<const float*>(smem + OFF_P + (t % kPBufs) * kPBufBytes + kPAlphaOff)[h];
       if (__any_sync(0xffffffffu, alpha != 1.f)) {
-        for (int c = 0; c < kDV; c += 16) {
-          uint32_t u[16];
-          tmem_ld16(tm + lane_off + TM_O + c, u);
+        for (int c = 0; c < kDV; c += 64) {
+          uint32_t u0[16], u1[16], u2[16], u3[16];
+          const uint32_t oa = tm + lane_off + TM_O + c;
+          tmem_ld16(oa, u0);
+          tmem_ld16(oa + 16, u1);
+          tmem_ld16(oa + 32, u2);
+          tmem_ld16(oa + 48, u3);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st16(tm + lane_off + TM_O + c, u);
+          for (int i = 0; i < 16; ++i) {
+            u0[i] = __float_as_uint(__uint_as_float(u0[i]) * alpha);
+            u1[i] = __float_as_uint(__uint_as_float(u1[i]) * alpha);
+            u2[i] = __float_as_uint(__uint_as_float(u2[i]) * alpha);
+            u3[i] = __float_as_uint(__uint_as_float(u3[i]) * alpha);
+          }
+          tmem_st16(oa, u0);
+          tmem_st16(oa + 16, u1);
+          tmem_st16(oa + 32, u2);
+          tmem_st16(oa + 48, u3);
         }
         tmem_st_wait();
       }
       tc_fence_before();
       mbar_arrive(bar(B_CORR_DONE));
     }
-    // epilogue: O / l
+    // epilogue: O / l, 64 columns at a time, through this warp's 8 KiB of the
+    // (now idle) stage region so that the global stores are whole rows
     bool ok = wait_bar_warp(bar(B_FINAL), 0, abort_flag, a.error_word) && n_tiles > 0;
     const bool have_ml = wait_bar_warp(bar(B_ML_FULL), 0, abort_flag, a.error_word, true);
     ok = ok && have_ml;  // warp-uniform: gates the warp-collective TMEM loads below
@@ -535,55 +786,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const bool has_rows = ok && l > 0.f;  // per head (lane)
     const float inv_l = has_rows ? 1.f / l : 0.f;
     const float lse = has_rows ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    const bool write = h < a.H;
+    const uint32_t stg = sbase + OFF_STAGE + (uint32_t)wq * 8192u;
+    for (int c0 = 0; c0 < kDV; c0 += 64) {
+      uint32_t u[64];
+      if (ok) {
+        const uint32_t oa = tm + lane_off + TM_O + c0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_ld16p(oa + 16 * i, u + 16 * i);
+        tmem_ld_wait();
+      }
+      if (a.splits == 1) {
+        // bf16: a head's 64 columns are 8 chunks of 16 B, chunk k at k ^ (lane % 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            pk[i] = has_rows ? pack_bf16x2(__uint_as_float(u[8 * k + 2 * i]) * inv_l,
+                                           __uint_as_float(u[8 * k + 2 * i + 1]) * inv_l)
+                             : 0u;
+          st_shared_v4(stg + lane * 128 + ((k ^ (lane & 7)) << 4),
+                       make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // 4 heads x 128 B per instruction
+          const int row = 4 * i + (lane >> 3), k = lane & 7;
+          const uint4 v = ld_shared_v4(stg + row * 128 + ((k ^ (row & 7)) << 4));
+          const int head = wq * 32 + row;
+          if (head < a.H)
+            *reinterpret_cast<uint4*>(a.out + ((int64_t)r * a.H + head) * kDV + c0 + 8 * k) = v;
+        }
+        __syncwarp();
+      } else {
+        // fp32: 16 chunks of 16 B per head, chunk k at k ^ (lane % 16)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (has_rows)
+            v = make_uint4(__float_as_uint(__uint_as_float(u[4 * k]) * inv_l),
+                           __float_as_uint(__uint_as_float(u[4 * k + 1]) * inv_l),
+                           __float_as_uint(__uint_as_float(u[4 * k + 2]) * inv_l),
+                           __float_as_uint(__uint_as_float(u[4 * k + 3]) * inv_l));
+          st_shared_v4(stg + lane * 256 + ((k ^ (lane & 15)) << 4), v);
+        }
+        __syncwarp();
+        float* wo = a.ws_o + (((int64_t)r * a.splits + split) * kHeads + wq * 32) * kDV + c0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {  // 2 heads x 256 B per instruction
+          const int row = 2 * i + (lane >> 4), k = lane & 15;
+          const uint4 v = ld_shared_v4(stg + row * 256 + ((k ^ (row & 15)) << 4));
+          *reinterpret_cast<uint4*>(wo + (int64_t)row * kDV + 4 * k) = v;
+        }
+        __syncwarp();
+      }
+    }
     if (a.splits == 1) {
-      uint16_t* orow = a.out + ((int64_t)r * a.H + (write ? h : 0)) * kDV;
-      for (int c = 0; c < kDV; c += 16) {
-        uint32_t u[16];
-        if (ok) {
-          tmem_ld16(tm + lane_off + TM_O + c, u);
-          tmem_ld_wait();
-        }
-        uint32_t pk[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          pk[i] = has_rows ? pack_bf16x2(__uint_as_float(u[2 * i]) * inv_l,
-                                         __uint_as_float(u[2 * i + 1]) * inv_l)
-                           : 0u;
-        if (write) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-          dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
-      }
-      if (write && a.lse) a.lse[(int64_t)r * a.H + h] = lse;
+      if (h < a.H && a.lse) a.lse[(int64_t)r * a.H + h] = lse;
     } else {
-      float* orow = a.ws_o + (((int64_t)r * a.splits + split) * kHeads + h) * kDV;
-      for (int c = 0; c < kDV; c += 16) {
-        uint32_t u[16];
-        if (ok) {
-          tmem_ld16(tm + lane_off + TM_O + c, u);
-          tmem_ld_wait();
-        }
-        float4* dst = reinterpret_cast<float4*>(orow + c);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = has_rows ? make_float4(__uint_as_float(u[4 * i]) * inv_l,
-                                          __uint_as_float(u[4 * i + 1]) * inv_l,
-                                          __uint_as_float(u[4 * i + 2]) * inv_l,
-                                          __uint_as_float(u[4 * i + 3]) * inv_l)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
       a.ws_lse[((int64_t)r * a.splits + split) * kHeads + h] = lse;
     }
+    finish();
+    return;
+  } else {
+    finish();  // idle warps of warpgroup 0
+    return;
   }
-
-  if (err) atomicOr(a.error_word, err);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == 0) tmem_dealloc(tm, 512);
-  cluster_sync();
 }
 
 // Combine per-split normalised partials: o = sum_c w_c o_c / sum_c w_c with
@@ -645,7 +913,8 @@ hs_status get_encoder() {
   return HS_OK;
 }
 
-// 2-D bf16 tensor map over [rows][576], 128B swizzle, box = 64 columns x box_rows.
+// TMA tensor map over bf16 [rows][576], 128B swizzle, box = 64 columns x
+// box_rows (128: one request's queries; 1: KV rows for the 4-row gathers).
 hs_status encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
   if (get_encoder() != HS_OK) return HS_ERR_CUDA;
   cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
@@ -659,13 +928,30 @@ hs_status encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint3
   return cr == CUDA_SUCCESS ? HS_OK : HS_ERR_INVALID;
 }
 
+// Launch the decode kernel (+ the merge when splits > 1).  Arguments checked by the caller.
+hs_status launch_decode(AttnArgs& a, const CUtensorMap& kv_map, const void* q, int R,
+                        cudaStream_t s) {
+  CUtensorMap q_map;  // host-side encode only: safe inside stream capture
+  if (encode_rows_map(&q_map, q, (uint64_t)R * a.H, kHeads) != HS_OK) return HS_ERR_INVALID;
+  const int tiles = (a.K + kTile - 1) / kTile;
+  a.rows_per_split = ((tiles + a.splits - 1) / a.splits) * kTile;
+  mla_decode_kernel<<<dim3(2 * a.splits, R), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
+  HS_CUDA_TRY(cudaGetLastError());
+  if (a.splits > 1) {
+    merge_splits_kernel<<<dim3(a.H, R), 128, 0, s>>>(a.ws_o, a.ws_lse, a.splits, a.H, a.out,
+                                                     a.lse);
+    HS_CUDA_TRY(cudaGetLastError());
+  }
+  return HS_OK;
+}
+
 }  // namespace
 
 hs_status hs_attn_workspace_init(hs_pool* p) {
   p->attn_o = nullptr;
   p->attn_ml = nullptr;
-  p->attn_kv_maps = nullptr;
   p->attn_max_splits = 0;
+  p->attn_kv_maps = nullptr;
   if (p->d.row_elems != kD) return HS_OK;  // attention needs 576-wide rows; decode call rejects
   HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)kSmemBytes));
@@ -711,10 +997,10 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void*
   if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
     return HS_ERR_INVALID;
   const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
-  CUtensorMap q_map;  // host-side encode only: safe inside stream capture
-  if (encode_rows_map(&q_map, q, (uint64_t)p->d.num_requests * num_heads, kHeads) != HS_OK)
-    return HS_ERR_INVALID;
+  if (rows_in_layer > INT32_MAX) return HS_ERR_INVALID;
   AttnArgs a;
+  a.kv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p->kv_pool) +
+                                        (int64_t)layer * rows_in_layer * kD);
   a.row_ids = row_ids;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
@@ -725,20 +1011,9 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void*
   a.K = p->d.top_k;
   a.H = num_heads;
   a.splits = p->attn_max_splits;
-  const int tiles = (a.K + kTile - 1) / kTile;
-  a.rows_per_split = ((tiles + a.splits - 1) / a.splits) * kTile;
   a.scale_log2 = scale * 1.4426950408889634f;
-  cudaStream_t s = hs_stream(stream);
-  dim3 grid(2 * a.splits, p->d.num_requests);
-  mla_decode_kernel<<<grid, kThreads, kSmemBytes, s>>>(
-      static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q_map, a);
-  HS_CUDA_TRY(cudaGetLastError());
-  if (a.splits > 1) {
-    merge_splits_kernel<<<dim3(num_heads, p->d.num_requests), 128, 0, s>>>(
-        p->attn_o, p->attn_ml, a.splits, num_heads, a.out, lse);
-    HS_CUDA_TRY(cudaGetLastError());
-  }
-  return HS_OK;
+  return launch_decode(a, static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q,
+                       p->d.num_requests, hs_stream(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -816,12 +1091,11 @@ extern "C" hs_status hs_sparse_mla_decode_noalloc(const void* kv_rows, int64_t n
   if (splits > 1 && (int64_t)num_requests * splits > kNoAllocMaxUnits)
     splits = kNoAllocMaxUnits / num_requests;
   if (splits < min_splits) splits = min_splits;
-  CUtensorMap kv_map, q_map;  // host-side encodes only
-  if (encode_rows_map(&kv_map, kv_rows, (uint64_t)num_rows, 1) != HS_OK ||
-      encode_rows_map(&q_map, q, (uint64_t)num_requests * num_heads, kHeads) != HS_OK)
-    return HS_ERR_INVALID;
+  CUtensorMap kv_map;  // host-side encode only
+  if (encode_rows_map(&kv_map, kv_rows, (uint64_t)num_rows, 1) != HS_OK) return HS_ERR_INVALID;
   float* scratch = g_noalloc_ptr[dev];
   AttnArgs a;
+  a.kv = static_cast<const uint4*>(kv_rows);
   a.row_ids = row_ids;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
@@ -832,15 +1106,6 @@ extern "C" hs_status hs_sparse_mla_decode_noalloc(const void* kv_rows, int64_t n
   a.K = top_k;
   a.H = num_heads;
   a.splits = splits;
-  a.rows_per_split = ((tiles + splits - 1) / splits) * kTile;
   a.scale_log2 = scale * 1.4426950408889634f;
-  cudaStream_t s = hs_stream(stream);
-  mla_decode_kernel<<<dim3(2 * splits, num_requests), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
-  HS_CUDA_TRY(cudaGetLastError());
-  if (splits > 1) {
-    merge_splits_kernel<<<dim3(num_heads, num_requests), 128, 0, s>>>(a.ws_o, a.ws_lse, splits,
-                                                                      num_heads, a.out, lse);
-    HS_CUDA_TRY(cudaGetLastError());
-  }
-  return HS_OK;
+  return launch_decode(a, kv_map, q, num_requests, hs_stream(stream));
 }
