@@ -70,11 +70,6 @@ constexpr int kLoadThreads = kLoadWarps * 32;
 static_assert(kLoadThreads == 4 * 64, "loader mapping: 64 value chunks x 4 groups of 16 rows");
 constexpr int kRopeWarp = 1;
 constexpr int kMathWarp0 = 12;
-// Registers per thread after the split (setmaxnreg, per warpgroup).  The kernel
-// launches with 128 per thread (512 threads x 128 = the SM's 65536); the split
-// 72 + 152 + 152 + 136 sums to 4 x 128, so every increase can be granted.
-constexpr int kRegsWG0 = 72, kRegsLoad = 152, kRegsMath = 136;
-static_assert(kRegsWG0 + 2 * kRegsLoad + kRegsMath == 4 * 128, "register split");
 constexpr int kCbK = kD / 64;      // 9 swizzled 128-byte column blocks per K row
 constexpr int kChunksK = kD / 8;   // 72 16-byte chunks per K row
 
@@ -240,15 +235,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
       : "memory");
-}
-// Register budget of this warpgroup from here on (all its warps execute it).
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 // TMA: one box (64 columns x box rows) from (x, y) into dst.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -453,8 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // Common exit: report errors, free tensor memory once every role is done, and
   // keep the CTA alive until its peer no longer addresses it.  Each role runs
-  // it at its own end (the roles run under different register budgets, so
-  // their code paths do not join again).
+  // it at its own end.
   auto finish = [&]() {
     if (err) atomicOr(a.error_word, err);
     tc_fence_before();
@@ -464,8 +449,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();
   };
 
-  // Each role first sets its warpgroup's register budget (kRegsWG0 ...); the
-  // four warps of a warpgroup always take the same budget.
   if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoadWarps) {
     // ================= value-column loaders (both CTAs) =================
     const int lt = tid - kLoadWarp0 * 32;
