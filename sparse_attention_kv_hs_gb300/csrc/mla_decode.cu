@@ -61,15 +61,23 @@ constexpr int kTile = 64;          // KV rows per tile
 constexpr int kStages = 2;         // KV tile ring depth
 constexpr int kThreads = 512;
 // Warp roles (four warpgroups of four warps):
-//   warp 0       MMA issuer               warp 1 (CTA 0)  rope-block TMA gathers
-//   warps 2..3   idle                     warps 4..11     value-column loaders
+//   warp 0       MMA issuer               warp 1 (CTA 0)  Q load
+//   warps 2..3   idle                     warps 4..11     row loaders (CTA 0: TMA
+//                                         gathers; CTA 1: vector loads + fp16)
 //   warps 12..15 softmax (CTA 0) / rescale + epilogue (CTA 1)
 constexpr int kLoadWarp0 = 4;
 constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = kLoadWarps * 32;
 static_assert(kLoadThreads == 4 * 64, "loader mapping: 64 value chunks x 4 groups of 16 rows");
-constexpr int kRopeWarp = 1;
+constexpr int kQWarp = 1;
 constexpr int kMathWarp0 = 12;
+// Registers per thread after the split (setmaxnreg, per warpgroup): the loader
+// warps hold two tiles of loads in flight.  The kernel launches with 128 per
+// thread (512 threads x 128 = the SM's 65536); 64 + 168 + 168 + 112 sums to
+// 4 x 128, so every increase can be granted.
+constexpr int kRegsWG0 = 64, kRegsLoad = 168, kRegsMath = 112;
+static_assert(kRegsWG0 + 2 * kRegsLoad + kRegsMath == 4 * 128, "register split");
+static_assert(65536 / 512 == 128, "launch allocation per thread");
 constexpr int kCbK = kD / 64;      // 9 swizzled 128-byte column blocks per K row
 constexpr int kChunksK = kD / 8;   // 72 16-byte chunks per K row
 
@@ -107,25 +115,26 @@ static_assert(4 * 8192 <= kStages * kStageBytes, "epilogue staging");
 enum {
   B_KV_FULL = 0,     // [2] loader warps stored a tile -> MMA (both CTAs: K tile / V tile)
   B_KV_EMPTY = 2,    // [2] MMA commit -> loaders
-  B_S_FULL = 4,      // [2] score MMA commit -> softmax
-  B_S_EMPTY = 6,     // [2] softmax -> score MMA
-  B_P_EMPTY = 8,     // [4] (CTA 0) value MMA commit (multicast) -> softmax
-  B_P_FULL = 12,     // [4] (CTA 1) bulk copies complete_tx -> value MMA
-  B_Q_SMEM = 16,     // (CTA 0) TMA of Q landed in shared memory
-  B_Q_READY = 17,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loaders
-  B_RID = 18,        // loader warps staged this split's row ids
-  B_CORR_REQ = 19,   // (CTA 1) value MMA -> rescale warps
-  B_CORR_DONE = 20,  // (CTA 1) rescale warps -> value MMA
-  B_MMA_IDLE = 21,   // (CTA 1) commit: earlier P.V MMAs finished
-  B_ML_FULL = 22,    // (CTA 1) softmax's final m, l -> epilogue
-  B_FINAL = 23,      // MMA issuer's last commit
-  B_COUNT = 24
+  B_S_FULL = 4,      // [3] score MMA commit -> softmax
+  B_S_EMPTY = 7,     // [3] softmax -> score MMA
+  B_P_EMPTY = 10,    // [4] (CTA 0) value MMA commit (multicast) -> softmax
+  B_P_FULL = 14,     // [4] (CTA 1) bulk copies complete_tx -> value MMA
+  B_Q_SMEM = 18,     // (CTA 0) TMA of Q landed in shared memory
+  B_Q_READY = 19,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loaders
+  B_RID = 20,        // loader warps staged this split's row ids
+  B_CORR_REQ = 21,   // (CTA 1) value MMA -> rescale warps
+  B_CORR_DONE = 22,  // (CTA 1) rescale warps -> value MMA
+  B_MMA_IDLE = 23,   // (CTA 1) commit: earlier P.V MMAs finished
+  B_ML_FULL = 24,    // (CTA 1) softmax's final m, l -> epilogue
+  B_FINAL = 25,      // MMA issuer's last commit
+  B_COUNT = 26
 };
+constexpr int kSBufs = 3;  // S accumulators in TMEM (CTA 0)
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 
 // TMEM columns
 constexpr uint32_t TM_Q = 0;     // CTA 0: Q, 288 columns (bf16 pairs)
-constexpr uint32_t TM_S = 288;   // CTA 0: S, 2 x 64 columns
+constexpr uint32_t TM_S = 288;   // CTA 0: S, 3 x 64 columns
 constexpr uint32_t TM_O = 0;     // CTA 1: O, 512 columns
 
 constexpr uint32_t kIdescS = idesc_bf16(128, kTile, false, false);  // A (TMEM), B K-major
@@ -236,6 +245,19 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
       : "memory");
 }
+// Register budget of this warpgroup from here on (all four of its warps run
+// it).  The launch gives every thread kLaunchRegs; a budget above that is an
+// increase, one below a release (setmaxnreg.inc may only grow the allocation
+// and .dec may only shrink it).
+constexpr int kLaunchRegs = 65536 / kThreads;
+template <int N>
+__device__ __forceinline__ void regs_set() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
+  if constexpr (N > kLaunchRegs)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+  else if constexpr (N < kLaunchRegs)
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 // TMA: one box (64 columns x box rows) from (x, y) into dst.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
@@ -290,8 +312,8 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
 // (column block c/8 at +8192 each, row at +128, chunk c%8 at position
 // (c%8) ^ (row%8)).  Loader thread lt owns chunk c = lt % 64 of rows
 // 16*(lt/64) .. +15 of every tile, so its shared-memory offsets are fixed and
-// its row ids come in 16-byte reads.  A thread issues its loads for tile t+1
-// before it waits for that tile's stage to free up.
+// its row ids come in 16-byte reads.  Each thread keeps two tiles of loads in
+// flight (the loads for tile t+2 are issued as soon as tile t is stored).
 // TO_F16 converts the values to fp16 on the way.  A row id of -1 stores zeros.
 struct ValueLoader {
   const uint4* col;  // chunk c of row 0
@@ -366,10 +388,13 @@ __device__ __forceinline__ int load_values(const ValueLoader& L, int n_tiles, ui
     if (lane == 0) mbar_arrive(bar_full0 + 8u * s);
     return true;
   };
-  uint4 va[16];
-  for (int t = 0; t < n_tiles; ++t) {
-    L.issue(t, va);
+  uint4 va[16], vb[16];  // two tiles of loads in flight
+  if (n_tiles > 0) L.issue(0, va);
+  for (int t = 0; t < n_tiles; t += 2) {
+    if (t + 1 < n_tiles) L.issue(t + 1, vb);
     if (!put(t, va)) break;
+    if (t + 2 < n_tiles) L.issue(t + 2, va);
+    if (t + 1 < n_tiles && !put(t + 1, vb)) break;
   }
   // 0x4780 is bf16 65536: from there up (inf and NaN included) fp16 cannot hold it
   if (TO_F16 && ((vmax & 0xffffu) >= 0x4780u || (vmax >> 16) >= 0x4780u)) return HS_DEV_ERR_VALUE;
@@ -400,10 +425,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, tensor memory ---------------------------------
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      // loader warps (+ the rope-gather arm in CTA 0)
-      mbar_init(bar(B_KV_FULL + i), kLoadWarps + (rank == 0 ? 1 : 0));
+    for (int i = 0; i < kStages; ++i) {
+      // CTA 0: one arm (+ TMA bytes); CTA 1: one arrival per loader warp
+      mbar_init(bar(B_KV_FULL + i), rank == 0 ? 1 : kLoadWarps);
       mbar_init(bar(B_KV_EMPTY + i), 1);
+    }
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(bar(B_S_FULL + i), 1);
       mbar_init(bar(B_S_EMPTY + i), 128);
     }
@@ -449,8 +476,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();
   };
 
+  // Each role first sets its warpgroup's register budget (kRegsWG0 ...); the
+  // four warps of a warpgroup always take the same budget.
   if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoadWarps) {
     // ================= value-column loaders (both CTAs) =================
+    regs_set<kRegsLoad>();
     const int lt = tid - kLoadWarp0 * 32;
     {  // this split's row ids -> shared memory, validated once (-1 = no row)
       constexpr int kRidPer = (kMaxSplitRows + kLoadThreads - 1) / kLoadThreads;
@@ -477,52 +507,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_RID));
     }
-    if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word)) {
+    if (rank == 0) {
+      // CTA 0: the whole 576-column rows by TMA (written straight into the
+      // swizzled stage, one shared-memory pass).  Lanes 0..15 of the eight
+      // warps issue the 9 x 16 gathers of 4 rows; a row id of -1 reads past the
+      // tensor, which fills zeros.  The first tile waits for Q to leave the
+      // stage region.
+      const int lw = warp - kLoadWarp0;
+      if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word) &&
+          wait_bar_warp(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
+        for (int t = 0; t < n_tiles; ++t) {
+          const int s = t % kStages;
+          if (!wait_bar_warp(bar(B_KV_EMPTY + s), ((uint32_t)(t / kStages) & 1u) ^ 1u,
+                             abort_flag, a.error_word))
+            break;
+          if (lw == 0 && lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), kStageBytes);
+          if (lane < kTile / 4) {
+            const int32_t* rid = s_rid + t * kTile + 4 * lane;
+            const int y0 = rid[0] >= 0 ? rid[0] : a.rows_in_layer;
+            const int y1 = rid[1] >= 0 ? rid[1] : a.rows_in_layer;
+            const int y2 = rid[2] >= 0 ? rid[2] : a.rows_in_layer;
+            const int y3 = rid[3] >= 0 ? rid[3] : a.rows_in_layer;
+            const uint32_t dst = sbase + OFF_STAGE + s * kStageBytes + lane * 512;
+            for (int cb = lw; cb < kCbK; cb += kLoadWarps)
+              tma_gather4(dst + cb * kBlockBytes, &kv_map, cb * 64, y0, y1, y2, y3,
+                          bar(B_KV_FULL + s));
+          }
+          __syncwarp();
+        }
+      }
+    } else if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word)) {
+      // CTA 1: the 512 value columns by vector loads, converted to fp16
       const ValueLoader L(a.kv, s_rid, sbase + OFF_STAGE, lt);
-      if (rank == 0)
-        err |= load_values<false>(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), bar(B_Q_READY),
-                                  abort_flag, a.error_word);
-      else
-        err |= load_values<true>(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
-                                 a.error_word);
+      err |= load_values<true>(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
+                               a.error_word);
     }
     finish();
     return;
-  } else if (warp == kRopeWarp && rank == 0) {
-    // ================= Q load, then the rope column block (CTA 0) =================
+  } else if (warp == kQWarp && rank == 0) {
+    // ================= Q load (CTA 0) =================
+    regs_set<kRegsWG0>();
     if (lane == 0 && !*abort_flag) {  // Q[r] (128 rows) -> smem by TMA
       mbar_arrive_expect_tx(bar(B_Q_SMEM), kCbK * kQBlockBytes);
       for (int cb = 0; cb < kCbK; ++cb)
         tma_load_2d(sbase + OFF_STAGE + cb * kQBlockBytes, &q_map, cb * 64, r * a.H,
                     bar(B_Q_SMEM));
     }
-    // rope block (columns 512..575) of each tile: 16 gathers of 4 rows, one per
-    // lane 0..15; a row id of -1 reads past the tensor, which fills zeros
-    if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word) &&
-        wait_bar_warp(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
-      for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % kStages;
-        if (!wait_bar_warp(bar(B_KV_EMPTY + s), ((uint32_t)(t / kStages) & 1u) ^ 1u, abort_flag,
-                           a.error_word))
-          break;
-        if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), kBlockBytes);
-        __syncwarp();
-        if (lane < kTile / 4) {
-          const int32_t* rid = s_rid + t * kTile + 4 * lane;
-          const int y0 = rid[0] >= 0 ? rid[0] : a.rows_in_layer;
-          const int y1 = rid[1] >= 0 ? rid[1] : a.rows_in_layer;
-          const int y2 = rid[2] >= 0 ? rid[2] : a.rows_in_layer;
-          const int y3 = rid[3] >= 0 ? rid[3] : a.rows_in_layer;
-          tma_gather4(sbase + OFF_STAGE + s * kStageBytes + 8 * kBlockBytes + lane * 512, &kv_map,
-                      kDV, y0, y1, y2, y3, bar(B_KV_FULL + s));
-        }
-        __syncwarp();
-      }
-    }
     finish();
     return;
   } else if (warp == 0) {
     // ================= MMA issuer (the whole warp runs it; one elected lane issues) =================
+    regs_set<kRegsWG0>();
     if (rank == 0) {
       // B = K tile, K-major, 128B swizzle: column block cb at +cb*8192, K step
       // kk at +(kk%4)*32 inside the block; 8-row groups 1024 B apart
@@ -530,8 +565,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (wait_bar_all(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
         tc_fence_after();
         for (int t = 0; t < n_tiles; ++t) {
-          const int s = t % kStages, b = t & 1;
-          const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t >> 1) & 1u;
+          const int s = t % kStages, b = t % kSBufs;
+          const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t / kSBufs) & 1u;
           if (!wait_bar_all(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
           if (!wait_bar_all(bar(B_S_EMPTY + b), pb ^ 1u, abort_flag, a.error_word)) break;
           tc_fence_after();
@@ -599,6 +634,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return;
   } else if (warp >= kMathWarp0 && rank == 0) {
     // ================= softmax (CTA 0, warps 12..15, one thread per head) =================
+    regs_set<kRegsMath>();
     const int h = tid - kMathWarp0 * 32;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = wait_bar_warp(bar(B_Q_SMEM), 0, abort_flag, a.error_word);
@@ -631,8 +667,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;  // this warp's heads: 32 wq .. 32 wq + 31
     float m_used = -INFINITY, l_sum = 0.f;
     for (int t = 0; ok && t < n_tiles; ++t) {
-      const int b = t & 1;  // S buffer
-      const uint32_t pb = (uint32_t)(t >> 1) & 1u;
+      const int b = t % kSBufs;  // S buffer
+      const uint32_t pb = (uint32_t)(t / kSBufs) & 1u;
       const int pbuf_i = t % kPBufs;  // P buffer
       const uint32_t ppar = (uint32_t)(t / kPBufs) & 1u;
       const uint64_t valid =
@@ -640,29 +676,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ((uint64_t)__ballot_sync(0xffffffffu, s_rid[t * kTile + lane + 32] >= 0) << 32);
       if (!wait_bar_warp(bar(B_S_FULL + b), pb, abort_flag, a.error_word)) break;
       tc_fence_after();
-      float x[kTile];
-      {
-        uint32_t u[kTile];
-        const uint32_t sa = tm + lane_off + TM_S + b * kTile;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tmem_ld16p(sa + 16 * i, u + 16 * i);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < kTile; ++i) x[i] = __uint_as_float(u[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(B_S_EMPTY + b));
-      // max of the raw scores (scale > 0 keeps the order); rows without a valid
-      // id become -inf, which the exponent below turns into 0
+      const uint32_t sa = tm + lane_off + TM_S + b * kTile;
+      // Two passes over S in tensor memory, 32 columns at a time (few live
+      // registers): the tile max of the raw scores first (scale > 0 keeps the
+      // order; rows without a valid id do not count), then the exponents.
       float tmax = -INFINITY;
-      if (valid == ~0ull) {
 #pragma unroll
-        for (int i = 0; i < kTile; ++i) tmax = fmaxf(tmax, x[i]);
-      } else {
+      for (int half = 0; half < 2; ++half) {
+        uint32_t u[32];
+        tmem_ld16p(sa + 32 * half, u);
+        tmem_ld16p(sa + 32 * half + 16, u + 16);
+        tmem_ld_wait();
+        const uint32_t vbits = (uint32_t)(valid >> (32 * half));
+        if (vbits == ~0u) {
 #pragma unroll
-        for (int i = 0; i < kTile; ++i) {
-          x[i] = ((valid >> i) & 1) ? x[i] : -INFINITY;
-          tmax = fmaxf(tmax, x[i]);
+          for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, __uint_as_float(u[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if ((vbits >> i) & 1) tmax = fmaxf(tmax, __uint_as_float(u[i]));
         }
       }
       tmax *= a.scale_log2;
@@ -677,23 +709,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // P buffer t % kPBufs is free once the value CTA finished tile t - kPBufs
       if (!wait_bar_warp(bar(B_P_EMPTY + pbuf_i), ppar ^ 1u, abort_flag, a.error_word)) break;
       unsigned char* pbuf = smem + OFF_P + pbuf_i * kPBufBytes;
-      // p = 2^(scale_log2 * x - m_used).  m_used is -inf only while no valid row
-      // has been seen, and then every x is -inf too: adding -inf keeps p = 0.
-      const float neg_m = m_used == -INFINITY ? -INFINITY : -m_used;
+      // p = 2^(scale_log2 * x - m_used); invalid rows give p = 0.  m_used is -inf
+      // only while no valid row has been seen, and then every p is 0.
+      const float neg_m = -m_used;
+      const bool none_yet = m_used == -INFINITY;
 #pragma unroll
-      for (int kb = 0; kb < kTile / 8; ++kb) {
-        uint32_t pk[4];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t u[32];
+        tmem_ld16p(sa + 32 * half, u);
+        tmem_ld16p(sa + 32 * half + 16, u + 16);
+        tmem_ld_wait();
+        const uint32_t vbits = none_yet ? 0u : (uint32_t)(valid >> (32 * half));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float p0 = fast_exp2(fmaf(x[kb * 8 + 2 * i], a.scale_log2, neg_m));
-          const float p1 = fast_exp2(fmaf(x[kb * 8 + 2 * i + 1], a.scale_log2, neg_m));
-          l_sum += p0 + p1;
-          pk[i] = pack_f16x2(p0, p1);
+        for (int kb = 0; kb < 4; ++kb) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = kb * 8 + 2 * i;
+            float p0 = fast_exp2(fmaf(__uint_as_float(u[j]), a.scale_log2, neg_m));
+            float p1 = fast_exp2(fmaf(__uint_as_float(u[j + 1]), a.scale_log2, neg_m));
+            p0 = ((vbits >> j) & 1) ? p0 : 0.f;
+            p1 = ((vbits >> (j + 1)) & 1) ? p1 : 0.f;
+            l_sum += p0 + p1;
+            pk[i] = pack_f16x2(p0, p1);
+          }
+          // P [128 heads x 64 rows], K-major core matrices (head group, row group)
+          const int kbg = half * 4 + kb;
+          const uint32_t off = (uint32_t)(((h >> 3) * (kTile / 8) + kbg) * 128 + (h & 7) * 16);
+          *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        // P [128 heads x 64 rows], K-major core matrices (head group, row group)
-        const uint32_t off = (uint32_t)(((h >> 3) * (kTile / 8) + kb) * 128 + (h & 7) * 16);
-        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      tc_fence_before();
+      mbar_arrive(bar(B_S_EMPTY + b));  // S buffer b read out
       reinterpret_cast<float*>(pbuf + kPAlphaOff)[h] = alpha;
       const uint32_t any = __ballot_sync(0xffffffffu, rescale && t > 0);
       if (lane == 0) reinterpret_cast<uint32_t*>(pbuf + kPFlagOff + 16 * wq)[0] = any;
@@ -722,6 +769,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return;
   } else if (warp >= kMathWarp0) {
     // ================= rescale + epilogue (CTA 1, warps 12..15) =================
+    regs_set<kRegsMath>();
     const int h = tid - kMathWarp0 * 32;  // head = TMEM lane
     const int wq = warp & 3;              // this warp's TMEM lane quarter (heads 32wq ..)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -770,55 +818,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float inv_l = has_rows ? 1.f / l : 0.f;
     const float lse = has_rows ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
     const uint32_t stg = sbase + OFF_STAGE + (uint32_t)wq * 8192u;
-    for (int c0 = 0; c0 < kDV; c0 += 64) {
-      uint32_t u[64];
+    for (int c0 = 0; c0 < kDV; c0 += 32) {  // 32 columns at a time (few live registers)
+      uint32_t u[32];
       if (ok) {
         const uint32_t oa = tm + lane_off + TM_O + c0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) tmem_ld16p(oa + 16 * i, u + 16 * i);
+        tmem_ld16p(oa, u);
+        tmem_ld16p(oa + 16, u + 16);
         tmem_ld_wait();
       }
       if (a.splits == 1) {
-        // bf16: a head's 64 columns are 8 chunks of 16 B, chunk k at k ^ (lane % 8)
+        // bf16: a head's 32 columns are 4 chunks of 16 B, chunk k at k ^ (lane % 4)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
           uint32_t pk[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             pk[i] = has_rows ? pack_bf16x2(__uint_as_float(u[8 * k + 2 * i]) * inv_l,
                                            __uint_as_float(u[8 * k + 2 * i + 1]) * inv_l)
                              : 0u;
-          st_shared_v4(stg + lane * 128 + ((k ^ (lane & 7)) << 4),
+          st_shared_v4(stg + lane * 64 + ((k ^ (lane & 3)) << 4),
                        make_uint4(pk[0], pk[1], pk[2], pk[3]));
         }
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {  // 4 heads x 128 B per instruction
-          const int row = 4 * i + (lane >> 3), k = lane & 7;
-          const uint4 v = ld_shared_v4(stg + row * 128 + ((k ^ (row & 7)) << 4));
+        for (int i = 0; i < 4; ++i) {  // 8 heads x 64 B per instruction
+          const int row = 8 * i + (lane >> 2), k = lane & 3;
+          const uint4 v = ld_shared_v4(stg + row * 64 + ((k ^ (row & 3)) << 4));
           const int head = wq * 32 + row;
           if (head < a.H)
             *reinterpret_cast<uint4*>(a.out + ((int64_t)r * a.H + head) * kDV + c0 + 8 * k) = v;
         }
         __syncwarp();
       } else {
-        // fp32: 16 chunks of 16 B per head, chunk k at k ^ (lane % 16)
+        // fp32: 8 chunks of 16 B per head, chunk k at k ^ (lane % 8)
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < 8; ++k) {
           uint4 v = make_uint4(0u, 0u, 0u, 0u);
           if (has_rows)
             v = make_uint4(__float_as_uint(__uint_as_float(u[4 * k]) * inv_l),
                            __float_as_uint(__uint_as_float(u[4 * k + 1]) * inv_l),
                            __float_as_uint(__uint_as_float(u[4 * k + 2]) * inv_l),
                            __float_as_uint(__uint_as_float(u[4 * k + 3]) * inv_l));
-          st_shared_v4(stg + lane * 256 + ((k ^ (lane & 15)) << 4), v);
+          st_shared_v4(stg + lane * 128 + ((k ^ (lane & 7)) << 4), v);
         }
         __syncwarp();
         float* wo = a.ws_o + (((int64_t)r * a.splits + split) * kHeads + wq * 32) * kDV + c0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {  // 2 heads x 256 B per instruction
-          const int row = 2 * i + (lane >> 4), k = lane & 15;
-          const uint4 v = ld_shared_v4(stg + row * 256 + ((k ^ (row & 15)) << 4));
+        for (int i = 0; i < 8; ++i) {  // 4 heads x 128 B per instruction
+          const int row = 4 * i + (lane >> 3), k = lane & 7;
+          const uint4 v = ld_shared_v4(stg + row * 128 + ((k ^ (row & 7)) << 4));
           *reinterpret_cast<uint4*>(wo + (int64_t)row * kDV + 4 * k) = v;
         }
         __syncwarp();
@@ -832,7 +880,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     finish();
     return;
   } else {
-    finish();  // idle warps of warpgroup 0
+    regs_set<kRegsWG0>();  // idle warps of warpgroup 0
+    finish();
     return;
   }
 }
