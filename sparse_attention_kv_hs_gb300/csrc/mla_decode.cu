@@ -79,7 +79,6 @@ constexpr int kRegsWG0 = 64, kRegsLoad = 168, kRegsMath = 112;
 static_assert(kRegsWG0 + 2 * kRegsLoad + kRegsMath == 4 * 128, "register split");
 static_assert(65536 / 512 == 128, "launch allocation per thread");
 constexpr int kCbK = kD / 64;      // 9 swizzled 128-byte column blocks per K row
-constexpr int kChunksK = kD / 8;   // 72 16-byte chunks per K row
 
 constexpr uint32_t kBlockBytes = kTile * 128;              // one column block of a tile: 8192
 constexpr uint32_t kStageBytes = kCbK * kBlockBytes;       // 73728
@@ -268,17 +267,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// 16-byte global load through the read-only path, not kept in L1 (each row is
-// read once per CTA; the pair's second read of it hits L2).
-__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-// Same, at row_base + row * 1152 bytes (one KV row), row >= 0; the address is
-// formed inside the statement so it occupies no register beyond the load.
+// 16-byte global load at row_base + row * 1152 bytes (one KV row), row >= 0,
+// through the read-only path and not kept in L1 (each row is read once per
+// CTA; the pair's second read of it hits L2).  The address is formed inside
+// the statement so it occupies no register beyond the load.
 __device__ __forceinline__ uint4 ld_row_chunk(const uint4* row_base, int row) {
   uint4 v;
   asm volatile(
