@@ -30,6 +30,8 @@ DEV_ERR_DUPLICATE = 2
 DEV_ERR_CAPACITY = 4
 DEV_ERR_BLOCK = 8
 DEV_ERR_WAIT = 16
+DEV_ERR_INTERNAL = 32
+DEV_ERR_VALUE = 64
 
 EXPORTED = (
     "hs_pool_create", "hs_pool_destroy", "hs_pool_get_views", "hs_pool_reset",

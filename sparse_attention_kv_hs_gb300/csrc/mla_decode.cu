@@ -449,11 +449,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_holder), 512);
     tmem_relinquish();
   }
-  // Set-up above touches no input; from here on the previous kernel's results
-  // (row ids, KV rows, queries) are read, so wait for it, and let the next
-  // kernel start launching.
-  pdl_wait();
-  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -890,8 +885,6 @@ __global__ void __launch_bounds__(128) merge_splits_kernel(const float* __restri
                                                            int splits, int H,
                                                            uint16_t* __restrict__ out,
                                                            float* __restrict__ lse_out) {
-  pdl_wait();  // the decode kernel's partials
-  pdl_trigger();
   const int r = blockIdx.y, h = blockIdx.x;
   float mx = -INFINITY;
   for (int c = 0; c < splits; ++c) mx = fmaxf(mx, ws_lse[((int64_t)r * splits + c) * kHeads + h]);
@@ -966,29 +959,12 @@ hs_status launch_decode(AttnArgs& a, const CUtensorMap& kv_map, const void* q, i
   if (encode_rows_map(&q_map, q, (uint64_t)R * a.H, kHeads) != HS_OK) return HS_ERR_INVALID;
   const int tiles = (a.K + kTile - 1) / kTile;
   a.rows_per_split = ((tiles + a.splits - 1) / a.splits) * kTile;
-  // Both kernels are programmatic dependents of what precedes them on the
-  // stream: they may start launching while it drains and wait for it
-  // (griddepcontrol.wait) before reading its results.
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * a.splits, R);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, mla_decode_kernel, kv_map, q_map, a));
+  mla_decode_kernel<<<dim3(2 * a.splits, R), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
+  HS_CUDA_TRY(cudaGetLastError());
   if (a.splits > 1) {
-    cudaLaunchConfig_t mcfg = {};
-    mcfg.gridDim = dim3(a.H, R);
-    mcfg.blockDim = dim3(128);
-    mcfg.stream = s;
-    mcfg.attrs = attr;
-    mcfg.numAttrs = 1;
-    HS_CUDA_TRY(cudaLaunchKernelEx(&mcfg, merge_splits_kernel, (const float*)a.ws_o,
-                                   (const float*)a.ws_lse, a.splits, a.H, a.out, a.lse));
+    merge_splits_kernel<<<dim3(a.H, R), 128, 0, s>>>(a.ws_o, a.ws_lse, a.splits, a.H, a.out,
+                                                     a.lse);
+    HS_CUDA_TRY(cudaGetLastError());
   }
   return HS_OK;
 }

@@ -130,9 +130,6 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 template <int P_CT, int RV_CT>
 __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  // the attention kernel that follows may start launching now; it waits for
-  // this kernel's completion before it reads the row ids and rows
-  hs_ptx::pdl_trigger();
   const SmemPlan sp = smem_plan(a.K, a.B, a.P, a.sel_bits);
   int32_t* s_order = reinterpret_cast<int32_t*>(smem + sp.order);
   int32_t* s_sel_key = reinterpret_cast<int32_t*>(smem + sp.sel_key);

@@ -90,15 +90,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   return false;
 }
 
-// ---------------------------------------------------- programmatic launch
-// Wait until the preceding kernel of the stream has completed and its memory
-// is visible (a no-op when this kernel was not launched as a programmatic
-// dependent); let the next kernel of the stream start launching.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

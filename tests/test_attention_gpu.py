@@ -182,6 +182,68 @@ def test_out_of_pool_row_ids_are_excluded_and_flagged():
     pool.close()
 
 
+def _bf16_bits(x):
+    """float values -> bf16 bit patterns (round to nearest even)."""
+    f = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((f + 0x7FFF + ((f >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _zero_query_mean(pool, n):
+    """q = 0: every score is 0, so the output is the mean of the n rows' value columns."""
+    ids = np.arange(n, dtype=np.int32)[None]
+    q0 = np.zeros((1, 128, W.ROW_ELEMS), dtype=np.uint16)
+    got, _ = _decode(pool, 0, q0, ids, 128)
+    return got[0]
+
+
+def test_value_columns_at_the_fp16_range_edges():
+    """P.V runs in fp16: bf16 values up to 65280 in magnitude and down to 2^-24
+    (fp16 subnormals) are carried exactly; the mean over the rows comes out
+    within bf16 rounding of the fp64 mean (plus fp32 accumulation for the large
+    values)."""
+    rng = np.random.default_rng(11)
+    cases = [
+        (rng.choice([-65280.0, 65280.0, -40000.0, 32768.0, 1.5], size=(32, 512)), 65280.0 * 2.0 ** -20),
+        (rng.choice([-2.0 ** -20, 2.0 ** -20, 3 * 2.0 ** -18, 2.0 ** -24], size=(32, 512)), 0.0),
+    ]
+    for vals, slack in cases:
+        pool, rows = _pool_with_rows(32)
+        rows = rows[:32].copy()
+        rows[:, :512] = _bf16_bits(vals)
+        pool.kv_pool[0][:32].copy_(torch.from_numpy(rows.view(np.int16)).cuda())
+        got = _zero_query_mean(pool, 32)
+        ref = synth.bf16_to_f32(rows[:, :512]).astype(np.float64).mean(axis=0)
+        err = np.abs(got - ref)
+        assert np.all(err <= np.abs(ref) * 2.0 ** -8 + slack), float(err.max())
+        assert hs.hs_check_errors(pool.handle) == 0
+        pool.close()
+
+
+@pytest.mark.parametrize("bits", [0x4780, 0xC780, 0x7F80, 0xFF80, 0x7FC0])
+def test_value_outside_fp16_range_is_flagged(bits):
+    """A value element of magnitude >= 65536 (or inf / NaN) sets error bit VALUE."""
+    pool, rows = _pool_with_rows(64)
+    rows = rows[:64].copy()
+    rows[7, 100] = bits
+    pool.kv_pool[0][:64].copy_(torch.from_numpy(rows.view(np.int16)).cuda())
+    _zero_query_mean(pool, 64)
+    assert hs.hs_check_errors(pool.handle) == hs.DEV_ERR_VALUE
+    pool.close()
+
+
+def test_rope_columns_are_not_range_checked():
+    """Columns 512..575 only enter the scores (bf16 x bf16 -> fp32), not P.V."""
+    pool, rows = _pool_with_rows(64)
+    rows = rows[:64].copy()
+    rows[7, 520] = 0x4780  # 65536 in a rope column
+    pool.kv_pool[0][:64].copy_(torch.from_numpy(rows.view(np.int16)).cuda())
+    got = _zero_query_mean(pool, 64)
+    ref = synth.bf16_to_f32(rows[:, :512]).astype(np.float64).mean(axis=0)
+    _check(np.broadcast_to(got, (128, 512)), np.broadcast_to(ref, (128, 512)))
+    assert hs.hs_check_errors(pool.handle) == 0
+    pool.close()
+
+
 def test_graph_captured_decode_step():
     """RESOLVE + attention of one layer captured once and replayed per step."""
     w = W.make("attention", R=2, L=1, steps=5)

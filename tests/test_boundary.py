@@ -69,3 +69,18 @@ def test_null_arguments_are_rejected_without_a_gpu():
         hs.HS_ERR_INVALID
     assert lib.hs_check_errors(None, None) == hs.HS_ERR_INVALID
     assert lib.hs_step_advance(None, None) == hs.HS_ERR_INVALID
+
+
+def test_error_codes_match_the_header():
+    """The binding's status and device-error constants are the header's values."""
+    import sparse_attention_kv_hs_gb300 as hs
+    text = open(HEADER).read()
+    defines = {m.group(1): int(m.group(2)) for m in
+               re.finditer(r"#define\s+HS_DEV_ERR_([A-Z]+)\s+(\d+)", text)}
+    assert defines, "no HS_DEV_ERR_ defines found"
+    for name, value in defines.items():
+        assert getattr(hs, "DEV_ERR_" + name) == value, name
+    enum = {m.group(1): int(m.group(2)) for m in
+            re.finditer(r"\bHS_(OK|ERR_[A-Z]+)\s*=\s*(-?\d+)", text)}
+    for name, value in enum.items():
+        assert getattr(hs, "HS_" + name) == value, name
