@@ -36,6 +36,9 @@ struct hs_pool {
   int attn_max_splits;
   void* attn_kv_maps;  // host array of one TMA tensor map per layer (CUtensorMap)
 
+  size_t resolve_smem;          // RESOLVE's dynamic shared memory per CTA
+  int resolve_max_clusters[4];  // clusters of 1, 2, 4, 8 CTAs that run at once
+
   cudaEvent_t order_event;  // orders offload copies after main-stream work
   int64_t* host_off_mirror; // host copy of host_off (set-up calls only)
 };
@@ -56,4 +59,5 @@ hs_status hs_attn_workspace_init(hs_pool* pool);
 void hs_attn_workspace_free(hs_pool* pool);
 // Shared memory the RESOLVE kernel needs for these sizes; sets the kernel's
 // dynamic shared-memory limit (call once per pool, outside stream capture).
-hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes);
+// Also reports how many RESOLVE clusters of 1, 2, 4 and 8 CTAs fit at once.
+hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes, int max_clusters[4]);

@@ -25,11 +25,12 @@
 //   4. each miss writes slot_pos/stamp/out and its host row is copied from
 //      mapped pinned host memory into the slot's pool row with 16-byte
 //      vector loads and stores.
-// The copies are bound by how many host reads are in flight, which is capped
-// per SM, so a unit is served by a cluster of C CTAs (C = SMs / units, at most
-// 8): CTA 0 runs steps 1-3 and 4's metadata, the others wait at a cluster
-// barrier, fetch their share of the miss list from CTA 0's shared memory and
-// every CTA copies its share of the rows.
+// The copies are bound by the host link and by how many host reads each SM
+// keeps in flight, so a unit is served by a cluster of C CTAs (C = SMs /
+// units, at most 8).  CTA 0 runs steps 1-4 for the whole selection; the
+// others start the host reads of their share of the misses while CTA 0 is
+// still choosing victims (see resolve_kernel), so the link does not wait for
+// the metadata.
 #include "hs_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -61,10 +62,13 @@ struct ResolveArgs {
   int32_t layer_begin, R, K, B, P, max_pages, row_vec;
   int32_t sel_bits, kpt, bpt;
   int32_t copy_ctas;  // C: CTAs (a cluster) per unit
+  int32_t smem_bytes; // dynamic shared memory per CTA (tables + staging)
 };
 
+// Both layouts start with one mbarrier at offset 0, so each CTA of a cluster
+// can address its peers' barrier without knowing their layout.
 struct SmemPlan {
-  size_t order, sel_key, sel_j, miss_j, miss_p, victim, hot, flag, warp, ptab, total;
+  size_t bar, order, sel_key, sel_j, miss_j, miss_p, victim, hot, flag, warp, ptab, total;
 };
 
 constexpr int kMaxSmemPages = 4096;  // page-table rows up to this width are staged in smem
@@ -74,6 +78,7 @@ __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(
 __host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int sel_bits) {
   SmemPlan s;
   size_t o = 0;
+  s.bar = o;       o = 16;
   s.order = o;     o = align16(o + sizeof(int32_t) * B);
   s.sel_key = o;   o = align16(o + sizeof(int32_t) * (size_t(1) << sel_bits));
   s.sel_j = o;     o = align16(o + sizeof(int32_t) * (size_t(1) << sel_bits));
@@ -88,10 +93,47 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int sel_bits)
   return s;
 }
 
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-  return v;
+// Fetch CTAs: their share's misses (j, position, destination row id), the
+// scan scratch, then staging for as many rows as fit.
+struct FetchPlan {
+  size_t bar, j, p, dst, warp, stage;
+};
+
+__host__ __device__ inline FetchPlan fetch_plan(int S) {
+  FetchPlan f;
+  size_t o = 0;
+  f.bar = o;   o = 16;
+  f.j = o;     o = align16(o + sizeof(int32_t) * S);
+  f.p = o;     o = align16(o + sizeof(int32_t) * S);
+  f.dst = o;   o = align16(o + sizeof(int32_t) * S);
+  f.warp = o;  o = align16(o + sizeof(int32_t) * (kWarps + 8));
+  f.stage = o;
+  return f;
+}
+
+constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before giving up
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait (acquire, cluster scope) for phase `parity` of a local mbarrier
+// that peers arrive on remotely; false after kWaitNs.
+__device__ __forceinline__ bool wait_peer_bar(uint32_t bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (hs_ptx::mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 15) == 15) {
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitNs) {
+        return false;
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t hash_pos(int32_t p, int bits) {
@@ -125,11 +167,186 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return base + x - v;
 }
 
+// Copy rows from mapped pinned host memory into their pool rows: row i of the
+// list goes from host row src(i) to pool row dst(i) (dst < 0: skip).  Each
+// thread keeps kCopyUnroll 16-byte loads in flight before it stores them.
+template <typename SrcF, typename DstF>
+__device__ __forceinline__ void copy_host_rows(const uint4* hsrc, uint4* kdst, int rv, int i_lo,
+                                               int i_hi, SrcF src, DstF dst) {
+  const int64_t total = (int64_t)(i_hi - i_lo) * rv;
+  for (int64_t base = threadIdx.x; base < total; base += (int64_t)kThreads * kCopyUnroll) {
+    uint4 v[kCopyUnroll];
+    int64_t d[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t c = base + (int64_t)u * kThreads;
+      d[u] = -1;
+      if (c < total) {
+        const int ii = (int)(c / rv);
+        const int e = (int)(c - (int64_t)ii * rv);
+        const int32_t row = dst(i_lo + ii);
+        if (row >= 0) {
+          v[u] = __ldcs(hsrc + (int64_t)src(i_lo + ii) * rv + e);
+          d[u] = (int64_t)row * rv + e;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u)
+      if (d[u] >= 0) kdst[d[u]] = v[u];
+  }
+}
+
+// Host rows 0 .. n-1 of a list -> shared-memory staging (row i at stage +
+// i * rv * 16), kCopyUnroll 16-byte loads in flight per thread.  (Vector loads
+// through registers: asynchronous cp.async copies from mapped host memory keep
+// far fewer reads in flight per SM.)
+template <typename SrcF>
+__device__ __forceinline__ void stage_host_rows(const uint4* hsrc, unsigned char* stage, int rv,
+                                                int n, SrcF src) {
+  uint4* st = reinterpret_cast<uint4*>(stage);
+  const int total = n * rv;
+  for (int base = threadIdx.x; base < total; base += kThreads * kCopyUnroll) {
+    uint4 v[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int c = base + u * kThreads;
+      if (c < total) {
+        const int i = c / rv, e = c - i * rv;
+        v[u] = __ldcs(hsrc + (int64_t)src(i) * rv + e);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int c = base + u * kThreads;
+      if (c < total) st[c] = v[u];
+    }
+  }
+}
+
+// Staged rows -> their pool rows.
+template <typename DstF>
+__device__ __forceinline__ void unstage_rows(const unsigned char* stage, uint4* kdst, int rv,
+                                             int n, DstF dst) {
+  for (int v = threadIdx.x; v < n * rv; v += kThreads) {
+    const int i = v / rv, e = v - i * rv;
+    const int32_t row = dst(i);
+    if (row >= 0) kdst[(int64_t)row * rv + e] = reinterpret_cast<const uint4*>(stage)[v];
+  }
+}
+
 // P_CT / RV_CT: compile-time page size and row width (16-byte vectors) for the
 // common shape (256, 72 = 576 bf16); 0 = take them from the arguments.
+//
+// A unit is served by a cluster of C CTAs.  CTA 0 ("metadata") runs steps 1-4
+// for the whole selection.  With C > 1 the other C - 1 CTAs ("fetch") split
+// the selection between them, classify their share themselves (page table and
+// the position -> slot array answer "miss" without any unit-wide state; a
+// repeated position is served by its first occurrence only, which CTA 0
+// decides) and start the host reads of their misses into shared-memory
+// staging at once, so the host link is busy while CTA 0 is still choosing
+// victims.  Two signals, each a remote arrival on one mbarrier, order the
+// phases: (1) each fetch CTA tells CTA 0 it has read the position -> slot
+// array, which CTA 0 updates only after all have; (2) CTA 0 tells each fetch
+// CTA that every miss's row id is written, which says where its staged rows
+// go.  A fetch CTA waits for CTA 0 alone, never for another fetch CTA.  Rows
+// beyond a CTA's staging capacity are copied straight from host memory to
+// their slots after (2).  With C == 1, CTA 0 starts the host reads of a first
+// small batch (one 16-byte load per thread, held in registers) before it
+// chooses victims.
 template <int P_CT, int RV_CT>
 __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
+  const int tid = threadIdx.x;
+  const int C = a.copy_ctas;
+  const uint32_t crank = C > 1 ? hs_ptx::cluster_ctarank() : 0u;
+  const int r = blockIdx.x / C;
+  const int li = blockIdx.y;               // layer index within this call
+  const int l = a.layer_begin + li;        // absolute layer
+  const int64_t unit = (int64_t)l * a.R + r;
+  const int64_t call_unit = (int64_t)li * a.R + r;
+  const int K = a.K, B = a.B, P = P_CT ? P_CT : a.P;
+  const int rv = RV_CT ? RV_CT : a.row_vec;
+  const int32_t* topk = a.topk + call_unit * K;
+  int32_t* out = a.out_rows + call_unit * K;
+  const int32_t* ptab = a.page_table + (int64_t)r * a.max_pages;
+  int32_t* inv_u = a.inv + (int64_t)l * a.host_tokens + a.host_off[r];
+  const uint4* hsrc = a.host_pool + ((int64_t)l * a.host_tokens + a.host_off[r]) * rv;
+  uint4* kdst = a.kv_pool + (int64_t)l * a.blocks_per_layer * P * rv;
+  const int32_t ctx = a.ctx_len[r];
+  const int row_bytes = rv * 16;
+  const uint32_t my_bar = hs_ptx::smem_u32(smem);  // offset 0 in both layouts
+  if (C > 1) {
+    if (tid == 0) {
+      // CTA 0's barrier collects one arrival per fetch CTA; a fetch CTA's, one from CTA 0
+      hs_ptx::mbar_init(my_bar, crank == 0 ? C - 1 : 1);
+      hs_ptx::fence_mbar_init_cluster();
+    }
+    hs_ptx::cluster_sync();  // every barrier exists before any remote arrival
+  }
+
+  if (crank != 0) {
+    // ======================= fetch CTA (C > 1) =======================
+    const int F = C - 1, f = (int)crank - 1;
+    const int S = (K + F - 1) / F;
+    const int j_lo = f * S, j_hi = min(K, j_lo + S);
+    const int kptf = (S + kThreads - 1) / kThreads;  // <= kpt <= 8
+    const FetchPlan fp = fetch_plan(S);
+    int32_t* f_j = reinterpret_cast<int32_t*>(smem + fp.j);
+    int32_t* f_p = reinterpret_cast<int32_t*>(smem + fp.p);
+    int32_t* f_dst = reinterpret_cast<int32_t*>(smem + fp.dst);
+    int* s_warp = reinterpret_cast<int*>(smem + fp.warp);
+    const int cap = (int)((a.smem_bytes - (int64_t)fp.stage) / row_bytes);
+
+    // classify this CTA's share: a miss is a valid position that is neither
+    // resident nor in the hot buffer
+    const int j0 = j_lo + tid * kptf;
+    int32_t my_p[8];
+    uint32_t miss_mask = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = j0 + q;
+      my_p[q] = -1;
+      if (q >= kptf || j >= j_hi) continue;
+      const int32_t p = topk[j];
+      my_p[q] = p;
+      if (p < 0 || p >= ctx) continue;
+      if (ptab[p / P] >= 0) continue;
+      if (inv_u[p] < 0) miss_mask |= 1u << q;
+    }
+    int n_local;
+    int mi = block_exclusive_scan(__popc(miss_mask), s_warp, &n_local);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (miss_mask & (1u << q)) {
+        f_j[mi] = j0 + q;
+        f_p[mi] = my_p[q];
+        ++mi;
+      }
+    __syncthreads();
+    // (1) this CTA is done reading the position -> slot array
+    if (tid == 0) hs_ptx::mbar_arrive_remote(hs_ptx::mapa(my_bar, 0));
+    const int n_stage = min(n_local, cap);
+    stage_host_rows(hsrc, smem + fp.stage, rv, n_stage, [&](int i) { return f_p[i]; });
+    // (2) CTA 0 has written the row id of every miss
+    int* s_ok = s_warp + kWarps;
+    if (tid == 0) *s_ok = wait_peer_bar(my_bar, 0) ? 1 : 0;
+    __syncthreads();
+    const bool ok = *s_ok != 0;
+    if (ok) {
+      for (int i = tid; i < n_local; i += kThreads) f_dst[i] = __ldcg(out + f_j[i]);
+      __syncthreads();
+      unstage_rows(smem + fp.stage, kdst, rv, n_stage, [&](int i) { return f_dst[i]; });
+      copy_host_rows(hsrc, kdst, rv, n_stage, n_local, [&](int i) { return f_p[i]; },
+                     [&](int i) { return f_dst[i]; });
+    } else if (tid == 0) {
+      atomicOr(a.error_word, HS_DEV_ERR_WAIT);
+    }
+    hs_ptx::cluster_sync();  // no CTA leaves while a peer may still address it
+    return;
+  }
+
+  // ======================= metadata CTA =======================
   const SmemPlan sp = smem_plan(a.K, a.B, a.P, a.sel_bits);
   int32_t* s_order = reinterpret_cast<int32_t*>(smem + sp.order);
   int32_t* s_sel_key = reinterpret_cast<int32_t*>(smem + sp.sel_key);
@@ -142,35 +359,16 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   int* s_warp = reinterpret_cast<int*>(smem + sp.warp);
   int32_t* s_ptab = reinterpret_cast<int32_t*>(smem + sp.ptab);
   int* s_err = s_warp + kWarps;
-
-  const int tid = threadIdx.x;
-  const int C = a.copy_ctas;
-  const uint32_t crank = C > 1 ? hs_ptx::cluster_ctarank() : 0u;
-  const int r = blockIdx.x / C;
-  const int li = blockIdx.y;               // layer index within this call
-  const int l = a.layer_begin + li;        // absolute layer
-  const int64_t unit = (int64_t)l * a.R + r;
-  const int64_t call_unit = (int64_t)li * a.R + r;
-  const int K = a.K, B = a.B, P = P_CT ? P_CT : a.P;
   const int hot_per_req = B / P;
   const int sel_mask = (1 << a.sel_bits) - 1;
-
-  const int32_t* topk = a.topk + call_unit * K;
-  int32_t* out = a.out_rows + call_unit * K;
   int32_t* g_slot_pos = a.slot_pos + unit * B;
   int32_t* g_stamp = a.slot_stamp + unit * B;
   int32_t* g_order = a.lru_order + unit * B;
-  const int32_t* ptab = a.page_table + (int64_t)r * a.max_pages;
-
   const int32_t step = *a.d_step;
-  const int32_t ctx = a.ctx_len[r];
 
   int err = 0;
-  int n_serve = 0;
   if (tid == 0) *s_err = 0;
-  if (crank == 0) {
   // ---- 0. load unit state, clear tables ---------------------------------
-  int32_t* inv_u = a.inv + (int64_t)l * a.host_tokens + a.host_off[r];
   for (int s = tid; s < B; s += kThreads) {
     s_order[s] = g_order[s];
     s_flag[s] = 0;
@@ -272,6 +470,18 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       ++mi;
     }
   // (the scan's trailing barrier also publishes s_flag from step 2)
+  // Alone on the unit: start the host reads of a first batch of misses, one
+  // 16-byte load per thread held in registers until the victims are known.
+  int n_early = 0;
+  uint4 early_v = make_uint4(0u, 0u, 0u, 0u);
+  if (C == 1) {
+    __syncthreads();  // s_miss_p complete
+    n_early = min(n_miss_total, kThreads / rv);
+    if (tid < n_early * rv) {
+      const int i = tid / rv, e = tid - i * rv;
+      early_v = __ldcs(hsrc + (int64_t)s_miss_p[i] * rv + e);
+    }
+  }
 
   // ---- 3. victims: untouched slots in (stamp, slot) order ---------------
   const int i0 = tid * a.bpt;
@@ -283,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   }
   int n_cand;
   int rank = block_exclusive_scan(__popc(cand_mask), s_warp, &n_cand);
-  n_serve = n_miss_total < n_cand ? n_miss_total : n_cand;
+  int n_serve = n_miss_total < n_cand ? n_miss_total : n_cand;
   if (n_miss_total > n_cand) err |= HS_DEV_ERR_CAPACITY;
 #pragma unroll 4
   for (int q = 0; q < 16; ++q) {
@@ -314,6 +524,14 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     if (used_mask & (1u << q)) g_order[kept + upos++] = i0 + q;
 
   // ---- 4. serve misses: metadata, row ids, log --------------------------
+  if (C > 1) {  // (1) every fetch CTA has read the position -> slot array
+    if (tid == 0) s_warp[kWarps + 1] = wait_peer_bar(my_bar, 0) ? 1 : 0;
+    __syncthreads();
+    if (!s_warp[kWarps + 1]) {  // never updated under a reader: serve nothing
+      err |= HS_DEV_ERR_WAIT;
+      n_serve = 0;
+    }
+  }
   int32_t* log = a.miss_log ? a.miss_log + call_unit * (int64_t)K * 3 : nullptr;
   for (int i = tid; i < n_miss_total; i += kThreads) {
     const int j = s_miss_j[i];
@@ -334,59 +552,29 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       out[j] = -1;
     }
   }
-
-  }  // end of CTA 0's metadata work
-
-  // ---- 5. copy missed rows: mapped pinned host -> hot slot in HBM --------
-  int* s_nserve = s_warp + kWarps + 1;
-  if (C > 1) {
-    if (crank == 0 && tid == 0) *s_nserve = n_serve;
-    hs_ptx::cluster_sync();  // CTA 0's miss list and hot blocks are complete
-    if (crank != 0) {
-      auto peer = [&](const void* p) { return hs_ptx::mapa(hs_ptx::smem_u32(p), 0); };
-      n_serve = (int)ld_cluster_u32(peer(s_nserve));
-      const int lo = (int)((int64_t)n_serve * crank / C), hi = (int)((int64_t)n_serve * (crank + 1) / C);
-      for (int i = lo + tid; i < hi; i += kThreads) {
-        s_miss_p[i] = (int32_t)ld_cluster_u32(peer(s_miss_p + i));
-        s_victim[i] = (int32_t)ld_cluster_u32(peer(s_victim + i));
-      }
-      for (int i = tid; i < hot_per_req; i += kThreads)
-        s_hot[i] = (int32_t)ld_cluster_u32(peer(s_hot + i));
-    }
-    __syncthreads();
-    hs_ptx::cluster_sync();  // every CTA holds its share: CTA 0 may run ahead and exit
-  }
-  const int i_lo = (int)((int64_t)n_serve * crank / C);
-  const int i_hi = (int)((int64_t)n_serve * (crank + 1) / C);
-  const int rv = RV_CT ? RV_CT : a.row_vec;
-  const uint4* hsrc = a.host_pool + ((int64_t)l * a.host_tokens + a.host_off[r]) * rv;
-  uint4* kdst = a.kv_pool + (int64_t)l * a.blocks_per_layer * P * rv;
-  const int64_t total = (int64_t)(i_hi - i_lo) * rv;
-  for (int64_t base = tid; base < total; base += (int64_t)kThreads * kCopyUnroll) {
-    uint4 v[kCopyUnroll];
-    int64_t dst[kCopyUnroll];
-#pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u) {
-      const int64_t c = base + (int64_t)u * kThreads;
-      dst[u] = -1;
-      if (c < total) {
-        const int ii = (int)(c / rv);
-        const int e = (int)(c - (int64_t)ii * rv);
-        const int i = i_lo + ii;
-        const int32_t s = s_victim[i];
-        v[u] = __ldcs(hsrc + (int64_t)s_miss_p[i] * rv + e);
-        dst[u] = ((int64_t)s_hot[s / P] * P + s % P) * rv + e;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u)
-      if (dst[u] >= 0) kdst[dst[u]] = v[u];
-  }
-
-  if (crank == 0 && tid == 0 && a.miss_count) a.miss_count[call_unit] = n_serve;
+  if (tid == 0 && a.miss_count) a.miss_count[call_unit] = n_serve;
   if (err) atomicOr(s_err, err);
   __syncthreads();
   if (tid == 0 && *s_err) atomicOr(a.error_word, *s_err);
+
+  if (C > 1) {  // (2) every miss's row id is written
+    if (tid == 0)
+      for (int c = 1; c < C; ++c) hs_ptx::mbar_arrive_remote(hs_ptx::mapa(my_bar, (uint32_t)c));
+    hs_ptx::cluster_sync();  // no CTA leaves while a peer may still address it
+    return;
+  }
+  // ---- 5. alone: copy the missed rows into their slots ------------------
+  auto slot_row = [&](int i) -> int32_t {
+    if (i >= n_serve) return -1;
+    const int32_t s = s_victim[i];
+    return s_hot[s / P] * P + s % P;
+  };
+  if (tid < n_early * rv) {
+    const int i = tid / rv, e = tid - i * rv;
+    const int32_t row = slot_row(i);
+    if (row >= 0) kdst[(int64_t)row * rv + e] = early_v;
+  }
+  copy_host_rows(hsrc, kdst, rv, n_early, n_serve, [&](int i) { return s_miss_p[i]; }, slot_row);
 }
 
 int ceil_log2(int64_t x) {
@@ -397,18 +585,47 @@ int ceil_log2(int64_t x) {
 
 }  // namespace
 
-hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes) {
+hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes, int max_clusters[4]) {
   const int sel_bits = ceil_log2(2 * (int64_t)K) < 5 ? 5 : ceil_log2(2 * (int64_t)K);
-  const size_t smem = smem_plan(K, B, P, sel_bits).total;
-  *smem_bytes = smem;
+  const size_t tables = smem_plan(K, B, P, sel_bits).total;
   int dev = 0, optin = 0;
   HS_CUDA_TRY(cudaGetDevice(&dev));
   HS_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-  if (smem > (size_t)optin) return HS_ERR_INVALID;  // K and B too large for one CTA
+  if (tables > (size_t)optin || fetch_plan(K).stage > (size_t)optin)
+    return HS_ERR_INVALID;  // K and B too large for one CTA
+  // One CTA per SM either way (1024 threads): what the tables leave is staging.
+  const size_t smem = (size_t)optin;
+  *smem_bytes = smem;
   HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<256, 72>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<0, 0>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  // How many clusters of 1, 2, 4 and 8 CTAs can run at once: a launch whose
+  // clusters do not all fit runs in waves, so the launch picks a size that fits.
+  int sms = 0, per_sm = 0;
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  HS_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, resolve_kernel<256, 72>,
+                                                            kThreads, smem));
+  max_clusters[0] = sms * per_sm;
+  for (int i = 1; i < 4; ++i) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(1 << i) * 64u);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1u << i;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, resolve_kernel<256, 72>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    max_clusters[i] = n;
+  }
   return HS_OK;
 }
 
@@ -447,10 +664,17 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
   if (a.kpt > 8 || a.bpt > 16) return HS_ERR_INVALID;
   // The kernel's dynamic shared-memory limit was raised by hs_pool_create
   // (hs_resolve_configure): nothing here may call outside the stream.
-  const size_t smem = smem_plan(a.K, a.B, a.P, a.sel_bits).total;
-  // copy helpers per unit: enough CTAs to put every SM to work on the copies
-  int C = p->num_sms / (a.R * num_layers);
-  C = C >= 8 ? 8 : C >= 4 ? 4 : C >= 2 ? 2 : 1;
+  const size_t smem = p->resolve_smem;
+  a.smem_bytes = (int32_t)smem;
+  // CTAs per unit: the largest cluster size (8, 4, 2) whose clusters, one per
+  // unit, all run at once; else one CTA per unit
+  const int64_t units = (int64_t)a.R * num_layers;
+  int C = 1;
+  for (int i = 3; i >= 1; --i)
+    if (units * (1 << i) <= p->num_sms && units <= p->resolve_max_clusters[i]) {
+      C = 1 << i;
+      break;
+    }
   a.copy_ctas = C;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.R * C, num_layers);
