@@ -5,8 +5,12 @@ One step = one decode step of the "attention" workload (32 requests x 2
 sparse layers, ctx 65536, top-K 2048, B 4096, 128 heads; 70% step-to-step
 selection reuse, the rest uniform): for each layer, RESOLVE (page table + LRU
 hot buffer + miss copies from pinned host memory) then sparse MLA decode
-attention over the K resolved rows, then the step counter advances.  Inputs
-(top-K traces, queries) are resident in HBM before the timed region.
+attention over the K resolved rows, then the step counter advances.  The step
+is one hs_decode_step call: layer l+1's RESOLVE runs on a copy stream beside
+layer l's attention ("precise prefetch").  Per-kernel rooflines come from a
+second timed pass of the same workload with the calls made one after another
+on one stream (CUDA events around each launch).  Inputs (top-K traces,
+queries) are resident in HBM before the timed region.
 
 Prints one JSON line (rank 0).  Metric: resolved top-K rows/s (value) and
 sparse-MLA decode tokens/s, with the dominant kernel's roofline fraction and
@@ -50,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="attention", choices=("attention", "resolve", "gather"))
     ap.add_argument("--e2e-steps", type=int, default=400)
+    ap.add_argument("--kernel-steps", type=int, default=500,
+                    help="steps of the sequential per-kernel timing pass")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -310,7 +316,9 @@ def run_ours(args):
 
     w = W.make(args.workload)
     w.req_base = replica_request_base(rank, w.R)
-    steps_total = args.warmup + args.steps
+    attention = args.workload == "attention"
+    kern_steps = min(args.kernel_steps, args.steps) if attention else 0
+    steps_total = args.warmup + args.steps + kern_steps
     topk_h, q_h = build_inputs(w, steps_total)
     scen = W.Scenario.build(w)
     pool = make_pool(hs, w, scen)
@@ -325,7 +333,7 @@ def run_ours(args):
     out_d = torch.empty((L, R, H, W.V_DIM), dtype=torch.bfloat16, device=dev)
     lse_d = torch.empty((L, R, H), dtype=torch.float32, device=dev)
     cnt_d = torch.zeros((steps_total, L, R), dtype=torch.int32, device=dev)
-    attention = args.workload == "attention"
+    copy_stream = torch.cuda.Stream(device=dev) if attention else None
     gather_d = None if attention else torch.empty((R * K, W.ROW_ELEMS), dtype=torch.int16,
                                                   device=dev)
     ph = pool.handle
@@ -358,12 +366,24 @@ def run_ours(args):
                 raise RuntimeError(f"libhs call failed at step {t}: {hs.status_string(st)}")
         lib.hs_step_advance(step_ptr, sptr)
 
+    def fused_step(t, ev=None):
+        """One hs_decode_step call: layer l+1's RESOLVE beside layer l's attention."""
+        st = lib.hs_decode_step(ph, 0, L, tk_base + t * tk_stride_t,
+                                q_base + (t % Q_DISTINCT) * q_stride_t, H, W.V_DIM, W.SCALE,
+                                step_ptr, rows_d.data_ptr(), out_d.data_ptr(), lse_d.data_ptr(),
+                                cnt_base + t * L * R * 4, sptr, copy_stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"hs_decode_step failed at step {t}: {hs.status_string(st)}")
+        lib.hs_step_advance(step_ptr, sptr)
+
+    step_fn = fused_step if attention else one_step
+
     peaks = load_peaks()
     h2d_peak = measure_h2d_peak(torch) if not args.profile else float("nan")
     host_read_peak = measure_host_read_peak(torch, hs, pool) if not args.profile else float("nan")
 
     for t in range(args.warmup):
-        one_step(t)
+        step_fn(t)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -371,29 +391,37 @@ def run_ours(args):
     if clocks:
         clocks.start()
         time.sleep(0.3)
-    n_ev = args.steps
+    # sequential steps timed launch by launch: the main region itself for the
+    # gather / resolve workloads, a second pass after it for the attention one
+    n_ev = args.steps if not attention else kern_steps
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(3)]
            for _ in range(n_ev)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
-        one_step(args.warmup + i, evs[i])
+        step_fn(args.warmup + i, None if attention else evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop() if clocks else None
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    misses_main = int(cnt_d[args.warmup:args.warmup + args.steps].sum().item())
+    k0 = args.warmup + args.steps if attention else args.warmup
+    if attention:
+        for i in range(kern_steps):
+            one_step(k0 + i, evs[i])
+        torch.cuda.synchronize()
     res_ms = sum(e[0][l].elapsed_time(e[1][l]) for e in evs for l in range(L))
     att_ms = sum(e[1][l].elapsed_time(e[2][l]) for e in evs for l in range(L))
     errs = hs.hs_check_errors(ph)
     if errs:
         raise RuntimeError(f"device error word set: {errs}")
-    misses = int(cnt_d[args.warmup:].sum().item())
+    misses = int(cnt_d[k0:k0 + n_ev].sum().item())
 
     rows_per_step = L * R * K
     value = weak_scaling_rate(rows_per_step, args.steps, world, elapsed_ms)
     tok_s = weak_scaling_rate(R, args.steps, world, elapsed_ms)
-    n_launch_res = args.steps * L
+    n_launch_res = max(n_ev, 1) * L
     res_avg_s = res_ms * 1e-3 / n_launch_res
     att_avg_s = att_ms * 1e-3 / n_launch_res
     miss_bytes_per_launch = misses * W.ROW_BYTES / n_launch_res
@@ -428,11 +456,9 @@ def run_ours(args):
             "traffic": ncu_traffic("gather.cu", args.workload), "avg_launch_us": att_avg_s * 1e6,
         }
     dominant = resolve_roof if res_ms >= att_ms else att_roof
-    gpu_launches = args.steps * (L * (1 + (1 if attention else 1)) + 1)
-    if attention:
-        splits = pool_splits(pool, R, K)
-        if splits > 1:
-            gpu_launches += args.steps * L  # split merge kernel
+    gpu_launches = args.steps * (2 * L + 1)  # RESOLVE + attention (or gather) per layer, step
+    if attention:  # + the split merge of each attention launch with more than one K split
+        gpu_launches += args.steps * sum(1 for s in decode_step_splits(pool, R, K, L) if s > 1)
 
     # ---- end to end: host buffers, H2D of the step's inputs, D2H of its outputs
     e2e = None
@@ -454,7 +480,10 @@ def run_ours(args):
                              f"{w.host_bytes() / 1e9:.1f} GB), no flush",
                        "parallelism": f"replicas x{world}"},
             "decode_tok_s": tok_s if attention else None,
-            "miss_rows_per_step": misses / args.steps,
+            "miss_rows_per_step": misses_main / args.steps,
+            "schedule": ("hs_decode_step: RESOLVE of layer l+1 on a copy stream beside layer l's "
+                         "attention; per-kernel rooflines from a sequential pass of "
+                         f"{n_ev} steps") if attention else "sequential, one stream",
             "roofline": dominant,
             "kernels": [resolve_roof, att_roof],
             "host_link_peak_gbs": h2d_peak,
@@ -476,6 +505,16 @@ def pool_splits(pool, R, K):
     sms = __import__("torch").cuda.get_device_properties(0).multi_processor_count
     tiles = (K + 63) // 64
     return max(1, min(tiles, sms // (2 * R)))
+
+
+def decode_step_splits(pool, R, K, L):
+    """K splits of each attention launch of one hs_decode_step (the library's
+    rule: a launch beside a RESOLVE gets the SMs RESOLVE's clusters leave)."""
+    sms = __import__("torch").cuda.get_device_properties(0).multi_processor_count
+    full = pool_splits(pool, R, K)
+    c_side = 2 if 3 * R <= sms else 1
+    s_side = max(1, (sms - c_side * R) // (2 * R))
+    return [min(full, s_side) if l + 1 < L else full for l in range(L)]
 
 
 def B_of(w):
@@ -507,18 +546,23 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
     g_d = None if attention else torch.empty((R * K, W.ROW_ELEMS), dtype=torch.int16, device=dev)
     g_h = None if attention else torch.empty(g_d.shape, dtype=torch.int16).pin_memory()
     sptr = stream.cuda_stream
+    copy_stream = torch.cuda.Stream(device=dev) if attention else None
 
     def step(t):
         tk_d.copy_(tk_pin[t], non_blocking=True)
         if attention:
             q_d.copy_(q_pin[t % Q_DISTINCT], non_blocking=True)
-        for l in range(L):
-            lib.hs_resolve(pool.handle, l, 1, tk_d[l].data_ptr(), pool.step.data_ptr(),
-                           rows_d[l].data_ptr(), None, None, sptr)
-            if attention:
-                lib.hs_sparse_mla_decode(pool.handle, l, q_d[l].data_ptr(), rows_d[l].data_ptr(), H,
-                                         W.V_DIM, W.SCALE, out_d[l].data_ptr(),
-                                         lse_d[l].data_ptr(), sptr)
+        if attention:  # the library's step call, as in the device-resident run
+            st = lib.hs_decode_step(pool.handle, 0, L, tk_d.data_ptr(), q_d.data_ptr(), H, W.V_DIM,
+                                    W.SCALE, pool.step.data_ptr(), rows_d.data_ptr(),
+                                    out_d.data_ptr(), lse_d.data_ptr(), None, sptr,
+                                    copy_stream.cuda_stream)
+            if st != 0:
+                raise RuntimeError(f"hs_decode_step failed: {hs.status_string(st)}")
+        else:
+            for l in range(L):
+                lib.hs_resolve(pool.handle, l, 1, tk_d[l].data_ptr(), pool.step.data_ptr(),
+                               rows_d[l].data_ptr(), None, None, sptr)
         if attention:
             out_h.copy_(out_d, non_blocking=True)
             lse_h.copy_(lse_d, non_blocking=True)

@@ -202,6 +202,39 @@ hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, const void* q,
                                int32_t v_dim, float scale, void* out,
                                float* lse, void* stream);
 
+/* One decode step over sparse layers layer_begin .. layer_begin+num_layers-1:
+ * for each layer i, RESOLVE (as hs_resolve) then sparse MLA decode attention
+ * over the resolved rows (as hs_sparse_mla_decode), with the same results as
+ * those calls made in that order, but with "precise prefetch": RESOLVE of
+ * layer i+1 -- its misses' host reads -- runs on `copy_stream` while layer i's
+ * attention runs on `stream`.  Page "59188saintaubert.com ... HiSparse",
+ * section 04: a synchronous resolve exposes 7-8 ms of host IO per token and
+ * prefetching with exact selections brings it to about 3 ms (section 03:
+ * prefetch alone adds 14-17% throughput); page "GLM 5.3 Optimizations, Part
+ * 1", section "Exploiting sparsity when needed": IndexShare gives one indexer
+ * layer per four sparse-MLA layers, so later layers' selections are known
+ * before the current layer's attention.
+ *   topk_idx     device int32 [num_layers][R][K]
+ *   q            device bf16 [num_layers][R][num_heads][576]
+ *   d_step       as for hs_resolve (not advanced here)
+ *   out_row_ids  device int32 [num_layers][R][K]
+ *   out          device bf16 [num_layers][R][num_heads][512]
+ *   lse          device float [num_layers][R][num_heads] or NULL
+ *   miss_count   device int32 [num_layers][R] or NULL
+ * `copy_stream` starts after the work queued on `stream` so far, and all of
+ * the step's work is ordered before later work on `stream`.  With copy_stream
+ * == stream (or one layer) the calls simply run in order on `stream`.
+ * Attention results may differ from hs_sparse_mla_decode's in the last bits
+ * (a launch beside a RESOLVE splits K into fewer parts).  Async,
+ * graph-capturable (copy_stream joins the capture through events); uses the
+ * pool's workspace and hand-off events, so steps on one pool must not overlap.
+ * Argument errors as for the two calls, checked before anything is queued. */
+hs_status hs_decode_step(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
+                         const int32_t* topk_idx, const void* q, int32_t num_heads,
+                         int32_t v_dim, float scale, const int32_t* d_step,
+                         int32_t* out_row_ids, void* out, float* lse,
+                         int32_t* miss_count, void* stream, void* copy_stream);
+
 /* Allocation-free variant of hs_sparse_mla_decode (no counterpart on the
  * pages: it exists for callers that cannot allocate device memory when they
  * decode -- an engine that handed all free HBM to its KV cache at start-up, an

@@ -38,7 +38,7 @@ EXPORTED = (
     "hs_set_request", "hs_map_page", "hs_load_page", "hs_resolve", "hs_gather",
     "hs_sparse_mla_decode", "hs_offload_prefix", "hs_commit_offload",
     "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
-    "hs_sparse_mla_decode_noalloc",
+    "hs_sparse_mla_decode_noalloc", "hs_decode_step",
 )
 
 
@@ -102,6 +102,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_check_errors": [p, ctypes.POINTER(i32)],
         "hs_host_read": [p, i64, p, p],
         "hs_sparse_mla_decode_noalloc": [p, i64, p, p, i32, i32, i32, i32, f32, p, p, p],
+        "hs_decode_step": [p, i32, i32, p, p, i32, i32, f32, p, p, p, p, p, p, p],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -222,6 +223,17 @@ def hs_sparse_mla_decode_noalloc(kv_rows, num_rows: int, q, row_ids, num_request
                                                num_requests, top_k, num_heads, v_dim, scale,
                                                _addr(out), _addr(lse), _stream(stream)),
            "hs_sparse_mla_decode_noalloc")
+
+
+def hs_decode_step(pool: int, layer_begin: int, num_layers: int, topk_idx, q, num_heads: int,
+                   v_dim: int, scale: float, d_step, out_row_ids, out, lse=None, miss_count=None,
+                   stream=None, copy_stream=None) -> None:
+    """RESOLVE + attention for each layer of one decode step; the next layer's
+    RESOLVE runs on `copy_stream` beside the current layer's attention."""
+    _check(load().hs_decode_step(pool, layer_begin, num_layers, _addr(topk_idx), _addr(q),
+                                 num_heads, v_dim, scale, _addr(d_step), _addr(out_row_ids),
+                                 _addr(out), _addr(lse), _addr(miss_count), _stream(stream),
+                                 _stream(copy_stream)), "hs_decode_step")
 
 
 def hs_offload_prefix(pool: int, req: int, page: int, main_stream, side_stream, done_event) -> None:

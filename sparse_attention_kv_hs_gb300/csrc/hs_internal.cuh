@@ -40,6 +40,7 @@ struct hs_pool {
   int resolve_max_clusters[4];  // clusters of 1, 2, 4, 8 CTAs that run at once
 
   cudaEvent_t order_event;  // orders offload copies after main-stream work
+  cudaEvent_t* step_events; // [L + 1] hand-offs between hs_decode_step's two streams
   int64_t* host_off_mirror; // host copy of host_off (set-up calls only)
 };
 
@@ -52,9 +53,18 @@ struct hs_pool {
 static inline cudaStream_t hs_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 // Launch wrappers implemented per translation unit.
+// max_cluster > 0 caps RESOLVE's CTAs per unit (to leave SMs to a kernel that
+// runs beside it); 0 = as many as fit.
 hs_status hs_launch_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
                             const int32_t* topk, const int32_t* d_step, int32_t* out_rows,
-                            int32_t* miss_count, int32_t* miss_log, cudaStream_t stream);
+                            int32_t* miss_count, int32_t* miss_log, int max_cluster,
+                            cudaStream_t stream);
+// Sparse MLA decode of one layer (arguments as hs_sparse_mla_decode);
+// max_splits > 0 caps the K splits per request (fewer SMs), 0 = the pool's.
+hs_status hs_launch_attention(hs_pool* pool, int32_t layer, const void* q,
+                              const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
+                              float scale, void* out, float* lse, int max_splits,
+                              cudaStream_t stream);
 hs_status hs_attn_workspace_init(hs_pool* pool);
 void hs_attn_workspace_free(hs_pool* pool);
 // Shared memory the RESOLVE kernel needs for these sizes; sets the kernel's

@@ -1010,9 +1010,9 @@ void hs_attn_workspace_free(hs_pool* p) {
   p->attn_kv_maps = nullptr;
 }
 
-extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void* q,
-                                          const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
-                                          float scale, void* out, float* lse, void* stream) {
+hs_status hs_launch_attention(hs_pool* p, int32_t layer, const void* q, const int32_t* row_ids,
+                              int32_t num_heads, int32_t v_dim, float scale, void* out, float* lse,
+                              int max_splits, cudaStream_t stream) {
   if (!p || !q || !row_ids || !out) return HS_ERR_INVALID;
   if (layer < 0 || layer >= p->d.num_layers || num_heads <= 0 || num_heads > kHeads ||
       v_dim != kDV || p->d.row_elems != kD || !(scale > 0.f) || p->attn_max_splits < 1 ||
@@ -1035,9 +1035,21 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void*
   a.K = p->d.top_k;
   a.H = num_heads;
   a.splits = p->attn_max_splits;
+  if (max_splits > 0 && max_splits < a.splits) {
+    const int tiles = (a.K + kTile - 1) / kTile;
+    const int min_splits = (tiles * kTile + kMaxSplitRows - 1) / kMaxSplitRows;
+    a.splits = max_splits > min_splits ? max_splits : min_splits;
+  }
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_decode(a, static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q,
-                       p->d.num_requests, hs_stream(stream));
+                       p->d.num_requests, stream);
+}
+
+extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void* q,
+                                          const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
+                                          float scale, void* out, float* lse, void* stream) {
+  return hs_launch_attention(p, layer, q, row_ids, num_heads, v_dim, scale, out, lse, 0,
+                             hs_stream(stream));
 }
 
 // ---------------------------------------------------------------------------

@@ -86,6 +86,11 @@ void free_pool(hs_pool* p) {
   cudaFree(p->error_word);
   hs_attn_workspace_free(p);
   if (p->order_event) cudaEventDestroy(p->order_event);
+  if (p->step_events) {
+    for (int i = 0; i <= p->d.num_layers; ++i)
+      if (p->step_events[i]) cudaEventDestroy(p->step_events[i]);
+    delete[] p->step_events;
+  }
   delete[] p->host_off_mirror;
   delete p;
 }
@@ -187,6 +192,17 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
     st = HS_ERR_CUDA;
     goto fail;
   }
+  p->step_events = new (std::nothrow) cudaEvent_t[L + 1]();
+  if (!p->step_events) {
+    st = HS_ERR_OOM;
+    goto fail;
+  }
+  for (int64_t i = 0; i <= L; ++i)
+    if (cudaEventCreateWithFlags(&p->step_events[i], cudaEventDisableTiming) != cudaSuccess) {
+      p->step_events[i] = nullptr;
+      st = HS_ERR_CUDA;
+      goto fail;
+    }
   init_tables_kernel<<<64, 256>>>(p->page_table, R * d.max_pages, p->hot_block, d.num_requests,
                                   d.hot_slots / d.page_tokens, p->ctx_len, p->host_off);
   reset_kernel<<<256, 256>>>(p->slot_pos, p->slot_stamp, p->lru_order, L * R, d.hot_slots,

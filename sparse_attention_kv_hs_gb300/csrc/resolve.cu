@@ -631,7 +631,8 @@ hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes, int max_
 
 hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
                             const int32_t* topk, const int32_t* d_step, int32_t* out_rows,
-                            int32_t* miss_count, int32_t* miss_log, cudaStream_t stream) {
+                            int32_t* miss_count, int32_t* miss_log, int max_cluster,
+                            cudaStream_t stream) {
   ResolveArgs a;
   a.topk = topk;
   a.d_step = d_step;
@@ -671,7 +672,8 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
   const int64_t units = (int64_t)a.R * num_layers;
   int C = 1;
   for (int i = 3; i >= 1; --i)
-    if (units * (1 << i) <= p->num_sms && units <= p->resolve_max_clusters[i]) {
+    if ((max_cluster <= 0 || (1 << i) <= max_cluster) && units * (1 << i) <= p->num_sms &&
+        units <= p->resolve_max_clusters[i]) {
       C = 1 << i;
       break;
     }
@@ -703,5 +705,5 @@ extern "C" hs_status hs_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_
   if (num_layers <= 0 || layer_begin < 0 || layer_begin + num_layers > pool->d.num_layers)
     return HS_ERR_INVALID;
   return hs_launch_resolve(pool, layer_begin, num_layers, topk_idx, d_step, out_row_ids,
-                           miss_count, miss_log, hs_stream(stream));
+                           miss_count, miss_log, 0, hs_stream(stream));
 }
