@@ -49,10 +49,12 @@ Q_DISTINCT = 64  # distinct decode queries cycled through (query values do not s
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 2000; the mixed workload: 120)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="attention", choices=("attention", "resolve", "gather"))
+    ap.add_argument("--workload", default="attention",
+                    choices=("attention", "resolve", "gather", "mixed"))
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--kernel-steps", type=int, default=500,
                     help="steps of the sequential per-kernel timing pass")
@@ -195,6 +197,22 @@ def measure_h2d_peak(torch, nbytes=1 << 30, reps=10):
     """Pinned host -> device cudaMemcpyAsync bandwidth, best of `reps` (GB/s)."""
     src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    best = 0.0
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del src, dst
+    return best
+
+
+def measure_d2h_peak(torch, nbytes=1 << 30, reps=10):
+    """Device -> pinned host cudaMemcpyAsync bandwidth, best of `reps` (GB/s)."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dst = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     best = 0.0
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -526,6 +544,177 @@ def workload_name(w):
             f"top-K {w.K}, B {w.B}" + (f", {w.heads} heads" if w.name == "attention" else ""))
 
 
+def run_mixed(args):
+    """The mixed-residency workload (128 requests x 1 sparse layer, contexts
+    log-uniform in [16384, 1048576], a quarter zero-residency and a quarter
+    fully resident, the rest with a 4096-token tail; K 2048, B 4096).  One step:
+    the page-table flips due at its boundary (committing the host copies queued
+    a step earlier), RESOLVE, the step counter, then ~6 requests each append a
+    finished 256-token page -- its rows are written into a resident block (the
+    stand-in for the model writing KV), mapped, queued for host offload on a
+    side stream, and the context grows.  Metric: resolved rows/s over the whole
+    step; the offload copies are timed on the side stream."""
+    import torch
+    import sparse_attention_kv_hs_gb300 as hs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    lib = hs.load()
+    steps_total = args.warmup + args.steps
+    w = W.make("mixed", steps=steps_total)
+    w.req_base = replica_request_base(rank, w.R)
+    scen = W.Scenario.build(w)
+    R, L, K, P = w.R, w.L, w.K, w.P
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+    topk = np.empty((steps_total, L, R, K), dtype=np.int32)
+    with cf.ThreadPoolExecutor(max_workers=16) as ex:
+        def one(r):
+            topk[:, :, r, :] = w.trace(r)
+        list(ex.map(one, range(R)))
+    pool = make_pool(hs, w, scen)
+    # rows of every page appended during the run, generated up front (device)
+    app = [(t, r, page, blk) for t in range(steps_total) for (r, page, blk) in scen.appends[t]]
+    app_rows = torch.empty((len(app), L, P, W.ROW_ELEMS), dtype=torch.int16, device=dev)
+    for i, (t, r, page, blk) in enumerate(app):
+        rows = np.stack([synth.rows(w.seed, w.req_base + r, l, page * P, P, threads=8)
+                         for l in range(L)])
+        app_rows[i].copy_(torch.from_numpy(rows.view(np.int16)))
+    topk_d = torch.from_numpy(topk).to(dev)
+    rows_d = torch.empty((R, K), dtype=torch.int32, device=dev)
+    cnt_d = torch.zeros((steps_total, R), dtype=torch.int32, device=dev)
+    offs = w.host_offsets()
+    ctx = w.ctx.astype(np.int64).copy()
+    ph = pool.handle
+    step_ptr = pool.step.data_ptr()
+    n_app = len(app)
+    ev_go = [torch.cuda.Event() for _ in range(n_app)]
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_app)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_app)]
+    for e in ev_b:  # torch creates events lazily; the library is handed raw handles
+        e.record(side)
+    torch.cuda.synchronize()
+    pending = {}
+    launches = [0]
+
+    def call(st, what):
+        if st != 0:
+            raise RuntimeError(f"{what} failed: {hs.status_string(st)}")
+
+    def one_step(t, ev_res=None):
+        for (r, page, blk) in scen.flips[t]:
+            i = pending.pop((r, page), None)
+            if i is not None:
+                call(lib.hs_commit_offload(ph, r, page, sptr, ev_b[i].cuda_event), "commit")
+            else:
+                call(lib.hs_map_page(ph, r, page, -1, sptr), "map_page")
+            launches[0] += 1
+        if ev_res is not None:
+            ev_res[0].record(stream)
+        call(lib.hs_resolve(ph, 0, 1, topk_d[t].data_ptr(), step_ptr, rows_d.data_ptr(),
+                            cnt_d[t].data_ptr(), None, sptr), "resolve")
+        if ev_res is not None:
+            ev_res[1].record(stream)
+        lib.hs_step_advance(step_ptr, sptr)
+        launches[0] += 2
+        for (r, page, blk) in scen.appends[t]:
+            i = app_index[(t, r, page)]
+            pool.kv_pool[0:L, blk * P:(blk + 1) * P].copy_(app_rows[i])  # model writes the page
+            call(lib.hs_map_page(ph, r, page, blk, sptr), "map_page")
+            ev_go[i].record(stream)
+            side.wait_event(ev_go[i])
+            ev_a[i].record(side)
+            call(lib.hs_offload_prefix(ph, r, page, sptr, side.cuda_stream, ev_b[i].cuda_event),
+                 "offload")
+            pending[(r, page)] = i
+            ctx[r] += P
+            call(lib.hs_set_request(ph, r, int(ctx[r]), int(offs[r]), sptr), "set_request")
+            launches[0] += 3  # map, offload, set_request (the page copy is a memcpy)
+
+    app_index = {(t, r, page): i for i, (t, r, page, blk) in enumerate(app)}
+    h2d_peak = measure_h2d_peak(torch) if not args.profile else float("nan")
+    d2h_peak = measure_d2h_peak(torch) if not args.profile else float("nan")
+    for t in range(args.warmup):
+        one_step(t)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = ClockSampler(local) if not args.profile else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    evr = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    launches[0] = 0
+    first_app = sum(len(scen.appends[t]) for t in range(args.warmup))
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        one_step(args.warmup + i, evr[i])
+    stream.wait_stream(side)  # the step's offload copies are part of the work
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop() if clocks else None
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    if hs.hs_check_errors(ph):
+        raise RuntimeError("device error word set in the mixed run")
+    res_ms = sum(e[0].elapsed_time(e[1]) for e in evr)
+    off_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(first_app, n_app)]
+    misses = int(cnt_d[args.warmup:].sum().item())
+    res_avg_s = res_ms * 1e-3 / args.steps
+    miss_bytes = misses * W.ROW_BYTES / args.steps
+    page_bytes = L * P * W.ROW_BYTES
+    off_avg_s = (sum(off_ms) / max(len(off_ms), 1)) * 1e-3
+    resolve_roof = {
+        "kernel": "resolve_kernel", "bound": "host_link",
+        "achieved": miss_bytes / res_avg_s / 1e9, "peak": h2d_peak, "unit": "GB/s",
+        "peak_source": "in-run pinned cudaMemcpyAsync H2D, 1 GiB, best of 10",
+        "frac": miss_bytes / res_avg_s / 1e9 / h2d_peak,
+        "traffic": ncu_traffic("resolve.cu", "mixed"), "avg_launch_us": res_avg_s * 1e6,
+        "miss_rows_per_launch": misses / args.steps,
+    }
+    off_roof = {
+        "kernel": "offload_page_kernel", "bound": "host_link",
+        "achieved": page_bytes / off_avg_s / 1e9 if off_ms else None, "peak": d2h_peak,
+        "unit": "GB/s", "peak_source": "in-run pinned cudaMemcpyAsync D2H, 1 GiB, best of 10",
+        "frac": page_bytes / off_avg_s / 1e9 / d2h_peak if off_ms else None,
+        "traffic": None, "avg_launch_us": off_avg_s * 1e6, "launches": len(off_ms),
+        "bytes_per_launch": page_bytes,
+    }
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": weak_scaling_rate(R * K * L, args.steps, world, elapsed_ms),
+            "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded generator; no dataset)",
+            "config": {"workload": (f"mixed: {R} requests x {L} sparse layer, ctx log-uniform "
+                                    f"16384..1048576, top-K {K}, B {w.B}, tail 4096; a quarter "
+                                    "zero-residency, a quarter fully resident; "
+                                    f"{w.appends_per_step} page appends + offloads per step"),
+                       "host_pool_gb": round(w.host_bytes() / 1e9, 1),
+                       "l2": "inputs larger than L2 (host pool and per-step misses), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "miss_rows_per_step": misses / args.steps,
+            "roofline": resolve_roof,
+            "kernels": [resolve_roof, off_roof],
+            "host_link_peak_gbs": h2d_peak, "host_link_d2h_peak_gbs": d2h_peak,
+            "e2e": None, "gpu_launches": launches[0], "clocks": clock_info,
+        }
+        print(json.dumps(line))
+    pool.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world):
     """Same step through the C ABI with HOST inputs/outputs: each step copies its
     top-K rows and queries from pinned host memory and reads the attention
@@ -632,8 +821,13 @@ def main(argv=None):
                           "sample": f"8 (request, layer) units x {steps} steps "
                                     f"(resolve + gather + fp64 attention), {secs:.1f} s"}))
         return
+    if args.steps is None:
+        args.steps = 120 if args.workload == "mixed" else 2000
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload == "mixed":
+        run_mixed(args)
         return
     run_ours(args)
 

@@ -169,31 +169,31 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 
 // Copy rows from mapped pinned host memory into their pool rows: row i of the
 // list goes from host row src(i) to pool row dst(i) (dst < 0: skip).  Each
-// thread keeps kCopyUnroll 16-byte loads in flight before it stores them.
+// thread keeps kCopyUnroll 16-byte loads in flight before it stores them; the
+// addresses are formed again for the stores rather than held in registers.
 template <typename SrcF, typename DstF>
 __device__ __forceinline__ void copy_host_rows(const uint4* hsrc, uint4* kdst, int rv, int i_lo,
                                                int i_hi, SrcF src, DstF dst) {
-  const int64_t total = (int64_t)(i_hi - i_lo) * rv;
-  for (int64_t base = threadIdx.x; base < total; base += (int64_t)kThreads * kCopyUnroll) {
+  const int total = (i_hi - i_lo) * rv;
+  for (int base = threadIdx.x; base < total; base += kThreads * kCopyUnroll) {
     uint4 v[kCopyUnroll];
-    int64_t d[kCopyUnroll];
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
-      const int64_t c = base + (int64_t)u * kThreads;
-      d[u] = -1;
+      const int c = base + u * kThreads;
       if (c < total) {
-        const int ii = (int)(c / rv);
-        const int e = (int)(c - (int64_t)ii * rv);
-        const int32_t row = dst(i_lo + ii);
-        if (row >= 0) {
-          v[u] = __ldcs(hsrc + (int64_t)src(i_lo + ii) * rv + e);
-          d[u] = (int64_t)row * rv + e;
-        }
+        const int i = i_lo + c / rv, e = c % rv;
+        if (dst(i) >= 0) v[u] = __ldcs(hsrc + (int64_t)src(i) * rv + e);
       }
     }
 #pragma unroll
-    for (int u = 0; u < kCopyUnroll; ++u)
-      if (d[u] >= 0) kdst[d[u]] = v[u];
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int c = base + u * kThreads;
+      if (c < total) {
+        const int i = i_lo + c / rv, e = c % rv;
+        const int32_t row = dst(i);
+        if (row >= 0) kdst[(int64_t)row * rv + e] = v[u];
+      }
+    }
   }
 }
 
