@@ -718,7 +718,10 @@ def run_mixed(args):
 def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world):
     """Same step through the C ABI with HOST inputs/outputs: each step copies its
     top-K rows and queries from pinned host memory and reads the attention
-    output (and lse) back; copies are inside the timed region."""
+    output (and lse) back; copies are inside the timed region.  A step's inputs
+    are copied after the previous step (a decode step's inputs come from the
+    one before); its output read-back runs on a second stream and overlaps the
+    next step (outputs are double-buffered)."""
     R, L, K, H = w.R, w.L, w.K, w.heads
     attention = w.name == "attention"
     steps = min(args.e2e_steps, topk_h.shape[0] - args.warmup)
@@ -728,23 +731,32 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
     tk_d = torch.empty((L, R, K), dtype=torch.int32, device=dev)
     q_d = torch.empty((L, R, H, W.ROW_ELEMS), dtype=torch.int16, device=dev)
     rows_d = torch.empty((L, R, K), dtype=torch.int32, device=dev)
-    out_d = torch.empty((L, R, H, W.V_DIM), dtype=torch.bfloat16, device=dev)
-    lse_d = torch.empty((L, R, H), dtype=torch.float32, device=dev)
-    out_h = torch.empty(out_d.shape, dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty(lse_d.shape, dtype=torch.float32).pin_memory()
-    g_d = None if attention else torch.empty((R * K, W.ROW_ELEMS), dtype=torch.int16, device=dev)
-    g_h = None if attention else torch.empty(g_d.shape, dtype=torch.int16).pin_memory()
+    if attention:
+        res_d = [(torch.empty((L, R, H, W.V_DIM), dtype=torch.bfloat16, device=dev),
+                  torch.empty((L, R, H), dtype=torch.float32, device=dev)) for _ in range(2)]
+        res_h = [(torch.empty((L, R, H, W.V_DIM), dtype=torch.bfloat16).pin_memory(),
+                  torch.empty((L, R, H), dtype=torch.float32).pin_memory()) for _ in range(2)]
+    else:
+        res_d = [(torch.empty((R * K, W.ROW_ELEMS), dtype=torch.int16, device=dev),) for _ in range(2)]
+        res_h = [(torch.empty((R * K, W.ROW_ELEMS), dtype=torch.int16).pin_memory(),)
+                 for _ in range(2)]
     sptr = stream.cuda_stream
     copy_stream = torch.cuda.Stream(device=dev) if attention else None
+    d2h_stream = torch.cuda.Stream(device=dev)
+    done = [torch.cuda.Event() for _ in range(2)]    # step wrote result buffer i
+    read = [torch.cuda.Event() for _ in range(2)]    # host copy of buffer i finished
 
     def step(t):
+        i = t % 2
         tk_d.copy_(tk_pin[t], non_blocking=True)
         if attention:
             q_d.copy_(q_pin[t % Q_DISTINCT], non_blocking=True)
+        if t >= 2:
+            stream.wait_event(read[i])  # buffer i's previous result has been read back
         if attention:  # the library's step call, as in the device-resident run
             st = lib.hs_decode_step(pool.handle, 0, L, tk_d.data_ptr(), q_d.data_ptr(), H, W.V_DIM,
                                     W.SCALE, pool.step.data_ptr(), rows_d.data_ptr(),
-                                    out_d.data_ptr(), lse_d.data_ptr(), None, sptr,
+                                    res_d[i][0].data_ptr(), res_d[i][1].data_ptr(), None, sptr,
                                     copy_stream.cuda_stream)
             if st != 0:
                 raise RuntimeError(f"hs_decode_step failed: {hs.status_string(st)}")
@@ -752,13 +764,15 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
             for l in range(L):
                 lib.hs_resolve(pool.handle, l, 1, tk_d[l].data_ptr(), pool.step.data_ptr(),
                                rows_d[l].data_ptr(), None, None, sptr)
-        if attention:
-            out_h.copy_(out_d, non_blocking=True)
-            lse_h.copy_(lse_d, non_blocking=True)
-        else:
-            lib.hs_gather(pool.handle, L - 1, rows_d[L - 1].data_ptr(), R * K, g_d.data_ptr(), sptr)
-            g_h.copy_(g_d, non_blocking=True)
+            lib.hs_gather(pool.handle, L - 1, rows_d[L - 1].data_ptr(), R * K,
+                          res_d[i][0].data_ptr(), sptr)
         lib.hs_step_advance(pool.step.data_ptr(), sptr)
+        done[i].record(stream)
+        d2h_stream.wait_event(done[i])
+        with torch.cuda.stream(d2h_stream):
+            for hb, db in zip(res_h[i], res_d[i]):
+                hb.copy_(db, non_blocking=True)
+        read[i].record(d2h_stream)
 
     for t in range(args.warmup):
         step(t)
@@ -769,6 +783,7 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
     a.record(stream)
     for i in range(steps):
         step(args.warmup + i)
+    stream.wait_stream(d2h_stream)  # the last read-back is inside the timed region
     b.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b), dist, dev)
@@ -777,7 +792,8 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
     h2d = L * R * K * 4 + (L * R * H * W.ROW_ELEMS * 2 if attention else 0)
     d2h = (L * R * H * (W.V_DIM * 2 + 4)) if attention else R * K * W.ROW_BYTES
     return {"value": weak_scaling_rate(L * R * K, steps, world, ms), "unit": "rows/s",
-            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "read-back of step t on a second stream beside step t+1"}
 
 
 # ----------------------------------------------------------------- reference arm
