@@ -11,6 +11,10 @@ with the CUDA library (``sparse_attention_kv_hs_gb300``) and never imports it.
   "GLM 5.3 Optimizations, Part 1: Hybrid HiSparse Offloading in vLLM",
   section "How it works"; the readings for points the pages leave open are
   listed in resolve_oracle.c.
+* ``policy_misses`` -- misses of one hot buffer under LRU, FIFO, random or
+  Belady replacement with RESOLVE's step structure (C, policy_sim.c), for the
+  replacement-policy comparison of page "59188saintaubert.com ... HiSparse",
+  section 04.
 * ``sparse_mla_decode`` -- attention of one decode query over exactly the K
   selected rows, in fp64 (softmax(scale * q k^T) v with v = the first 512
   columns of each 576-wide latent row).  The pages state the method is exact:
@@ -29,6 +33,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "resolve_oracle.c")
+_POLICY_SRC = os.path.join(_HERE, "policy_sim.c")
 _HDR = os.path.join(_HERE, "resolve_oracle.h")
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
@@ -40,11 +45,12 @@ ERR_RANGE, ERR_DUPLICATE, ERR_CAPACITY, ERR_BLOCK = 1, 2, 4, 8
 def build(force: bool = False) -> str:
     """Compile the C part of the oracle in place (plain C, gcc)."""
     stale = force or not os.path.exists(_LIB) or max(
-        os.path.getmtime(_SRC), os.path.getmtime(_HDR)) > os.path.getmtime(_LIB)
+        os.path.getmtime(_SRC), os.path.getmtime(_HDR),
+        os.path.getmtime(_POLICY_SRC)) > os.path.getmtime(_LIB)
     if stale:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared",
-                               "-ffp-contract=off", "-Wall", "-o", tmp, _SRC])
+                               "-ffp-contract=off", "-Wall", "-o", tmp, _SRC, _POLICY_SRC])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -72,6 +78,8 @@ def _load():
             lib.or_get_unit.argtypes = [p, i32, i32, p, p]
             lib.or_row_content.restype = i32
             lib.or_row_content.argtypes = [p, i32, i32, i32, p]
+            lib.ps_simulate.restype = i32
+            lib.ps_simulate.argtypes = [i32, i32, i32, i32, i32, p, ctypes.c_uint64, p]
             _lib = lib
     return _lib
 
@@ -146,6 +154,23 @@ class ResolveOracle:
         p = ctypes.c_int32(-1)
         self._lib.or_row_content(self._h, layer, req, int(row), ctypes.addressof(p))
         return p.value
+
+
+POLICIES = {"lru": 0, "fifo": 1, "random": 2, "belady": 3}
+
+
+def policy_misses(policy: str, trace, hot_slots: int, ctx: int, seed: int = 0) -> np.ndarray:
+    """Misses per step of one hot buffer of `hot_slots` slots over `trace`
+    ([steps][K] positions, -1 = skipped) under the named replacement policy
+    (page "59188saintaubert.com ... HiSparse", section 04 compares these)."""
+    tr = np.ascontiguousarray(trace, dtype=np.int32)
+    steps, K = tr.shape
+    out = np.zeros(steps, dtype=np.int32)
+    rc = _load().ps_simulate(POLICIES[policy], K, hot_slots, steps, ctx, _ptr(tr), seed,
+                             _ptr(out))
+    if rc != 0:
+        raise ValueError("ps_simulate: bad arguments")
+    return out
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
