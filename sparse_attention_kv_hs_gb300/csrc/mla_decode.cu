@@ -13,28 +13,26 @@
 // SM's tensor memory, so each (request, split-of-K) is handled by a CTA pair
 // (a cluster of 2):
 //   CTA 0 ("score"): Q lives in tensor memory (the A operand); S = Q K^T
-//     (M=128, N=64, K=576) over 64-row tiles goes to a double-buffered TMEM
-//     accumulator; 4 warps run the online softmax (one thread per head) and
+//     (M=128, N=64, K=576) over 64-row tiles goes to one of three TMEM
+//     accumulators; 4 warps run the online softmax (one thread per head) and
 //     write P in fp16 (11 significant bits; bf16 P would cost ~1.5e-3 relative
-//     error), which one bulk copy sends into CTA 1.
+//     error), which per-warp bulk copies send into CTA 1's P ring.
 //   CTA 1 ("value"): accumulates O += P V (M=128, N=256 x 2, V as an MN-major
 //     operand) with V in fp16 as well.  Its 4 epilogue warps rescale O when the
 //     running max moved (lazily: only when it grew by more than 2^8, so the
 //     rescale is rare and off the common path) and write the output through
 //     shared memory in coalesced rows.
-// Row loads.  Each CTA loads the tile rows it needs itself (CTA 0: all 576
-// columns, CTA 1: the 512 value columns), so the two stage rings never wait on
-// each other.  Eleven loader warps per CTA move the rows with 16-byte vector
-// loads into registers and store them into the 128B-swizzled operand layout;
-// a loader thread issues its loads for tile t+1 before it waits for the stage
-// to free up, so the loads overlap the MMAs.  (Plain vector loads move about
-// twice the bytes per SM-clock that TMA row gathers do for scattered 1152-byte
-// rows, and CTA 1 converts its values to fp16 on the way through registers.)
-// Q reaches CTA 0 by TMA (swizzled, then TMEM), each split's row ids are staged
-// in shared memory once by all loader warps, MMA descriptors are computed once
-// and advanced by constants, and every hand-off is an mbarrier.  With several
-// splits per request, each pair writes a normalised fp32 partial and its
-// log-sum-exp; a small merge kernel combines them.
+// Row loads.  Each CTA loads the tile rows it needs itself, so the two stage
+// rings never wait on each other: CTA 0 gathers the whole 576-column rows by
+// TMA (tile::gather4, 128-byte swizzle, straight into the operand layout);
+// CTA 1's eight loader warps move the 512 value columns with 16-byte vector
+// loads, converting them to fp16 through registers, with the loads for the
+// next tile issued before the stage frees up.  Q reaches CTA 0 by TMA
+// (swizzled, then TMEM), each split's row ids are staged in shared memory
+// once, MMA descriptors are computed once and advanced by constants, and
+// every hand-off is an mbarrier.  With several splits per request, each pair
+// writes a normalised fp32 partial and its log-sum-exp; a small merge kernel
+// combines them.
 //
 // Every wait is bounded: a wait that times out sets HS_DEV_ERR_WAIT in the
 // pool's error word and the CTA winds down (no further MMAs), frees its tensor
