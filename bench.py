@@ -265,10 +265,11 @@ def ncu_traffic(kernel_file, workload):
 
 # ----------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, seconds, units=2, steps_cap=None):
+def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0):
     """Run the CPU oracle (resolve + gather from host full KV + fp64 attention)
     over the first `units` (request, layer) units of the workload, step after
-    step, for about `seconds`.  Returns (rows resolved, elapsed s, steps)."""
+    step, for about `seconds` after `skip` untimed warm-up steps.  Returns
+    (rows resolved, elapsed s, steps) of the timed steps."""
     import oracle
     scen = W.Scenario.build(w)
     o = oracle.ResolveOracle(w.R, w.L, w.K, w.B, w.P, w.ctx_capacity(), scen.blocks_per_layer)
@@ -288,15 +289,17 @@ def oracle_sample(w, seconds, units=2, steps_cap=None):
     qs = {(r, l): synth.q(w.seed, w.req_base + r, l, 0, w.heads) for (r, l) in sel}
     rows_done, t0, t = 0, time.perf_counter(), 0
     while t < steps:
+        if t == skip:  # warm-up over: start the clock
+            rows_done, t0 = 0, time.perf_counter()
         for (r, l) in sel:
             rows, _, _ = o.resolve(l, r, tr[r][t, l], t)
             gathered = full[(r, l)][tr[r][t, l]]          # rows at the selected positions
             oracle.sparse_mla_decode(qs[(r, l)], gathered, rows >= 0, W.SCALE)
             rows_done += w.K
         t += 1
-        if time.perf_counter() - t0 >= seconds:
+        if t > skip and time.perf_counter() - t0 >= seconds:
             break
-    return rows_done, time.perf_counter() - t0, t
+    return rows_done, time.perf_counter() - t0, t - min(skip, t)
 
 
 def cpu_baseline(w, seconds):
@@ -809,8 +812,9 @@ def run_reference(args):
     w = W.make(args.workload)
     total = args.warmup + args.steps
     units = 2
-    # warm-up steps are run and discarded by timing only the last `steps`
-    rows, secs, done = oracle_sample(w, seconds=1e9, units=units, steps_cap=total)
+    # the warm-up steps run untimed, then `steps` timed steps
+    rows, secs, done = oracle_sample(w, seconds=1e9, units=units, steps_cap=total,
+                                     skip=args.warmup)
     per_step = secs / max(done, 1)
     value = units * w.K / per_step
     cores = os.cpu_count() or 1
