@@ -74,6 +74,8 @@ def _load():
                 f.argtypes = [p, i32, i32, i32]
             lib.or_resolve.restype = i32
             lib.or_resolve.argtypes = [p, i32, i32, p, i32, p, p, p]
+            lib.or_resolve_tokens.restype = i32
+            lib.or_resolve_tokens.argtypes = [p, i32, i32, i32, p, i32, p, p, p]
             lib.or_get_unit.restype = i32
             lib.or_get_unit.argtypes = [p, i32, i32, p, p]
             lib.or_row_content.restype = i32
@@ -138,6 +140,22 @@ class ResolveOracle:
         n = ctypes.c_int32(0)
         err = self._lib.or_resolve(self._h, layer, req, _ptr(topk), step, _ptr(out),
                                    _ptr(log), ctypes.addressof(n))
+        if err < 0:
+            raise ValueError("bad unit")
+        return out, log[: n.value].copy(), err
+
+    def resolve_tokens(self, layer: int, req: int, topk, step: int):
+        """One speculative-decoding step of one unit: topk[T][K] (T verify
+        tokens) -> (row_ids[T][K], miss_log[n][3] with j indexing the
+        flattened [T*K] list, err_bits)."""
+        topk = np.ascontiguousarray(topk, dtype=np.int32)
+        T = topk.shape[0]
+        assert topk.shape == (T, self.K)
+        out = np.empty((T, self.K), dtype=np.int32)
+        log = np.empty((T * self.K, 3), dtype=np.int32)
+        n = ctypes.c_int32(0)
+        err = self._lib.or_resolve_tokens(self._h, layer, req, T, _ptr(topk), step, _ptr(out),
+                                          _ptr(log), ctypes.addressof(n))
         if err < 0:
             raise ValueError("bad unit")
         return out, log[: n.value].copy(), err

@@ -27,6 +27,16 @@
  *     repeat of an earlier position in the same row is an input error (row id
  *     -1, error bit set); misses beyond the number of victims get row id -1
  *     and the capacity error bit.
+ * Speculative decoding (page "GLM 5.3 Optimizations, Part 1", sections
+ * "Composition with the rest of vLLM" and "Exploiting sparsity when needed":
+ * the verify steps share the request's hot state, and the hot buffer must
+ * hold every verify token's selection at once).  Reading: the T verify
+ * tokens' rows are resolved as one list, token after token; the whole list's
+ * hits are refreshed first and its misses served in list order, so a slot any
+ * token uses is pinned for the step; a position that an earlier token also
+ * selected takes no second slot -- it gets the row of its first occurrence
+ * (whatever that is: resident, hot, a served miss, or -1 if that miss found
+ * no slot); a repeat within one token's row stays an input error.
  */
 #include "resolve_oracle.h"
 
@@ -44,9 +54,9 @@ struct or_state {
   int32_t* slot_stamp;   /* [L][R][B] */
   int32_t** where;       /* [L*R] -> [ctx_cap[r]]: slot holding a position, or -1 */
   int32_t** seen;        /* [L*R] -> [ctx_cap[r]]: call serial of last sighting */
+  int32_t** seen_j;      /* [L*R] -> [ctx_cap[r]]: list index of that sighting */
   int32_t* serial;       /* [L*R] */
   /* per-call scratch */
-  int32_t* miss_j;       /* [K] */
   int32_t* cand;         /* [B] */
 };
 
@@ -71,11 +81,11 @@ or_state* or_create(int32_t R, int32_t L, int32_t K, int32_t B, int32_t P,
   s->slot_stamp = (int32_t*)malloc(sizeof(int32_t) * (size_t)L * R * B);
   s->where = (int32_t**)calloc((size_t)L * R, sizeof(int32_t*));
   s->seen = (int32_t**)calloc((size_t)L * R, sizeof(int32_t*));
+  s->seen_j = (int32_t**)calloc((size_t)L * R, sizeof(int32_t*));
   s->serial = (int32_t*)calloc((size_t)L * R, sizeof(int32_t));
-  s->miss_j = (int32_t*)malloc(sizeof(int32_t) * (size_t)K);
   s->cand = (int32_t*)malloc(sizeof(int32_t) * (size_t)B);
   if (!s->ctx || !s->ctx_cap || !s->page_table || !s->hot_block || !s->slot_pos ||
-      !s->slot_stamp || !s->where || !s->seen || !s->serial || !s->miss_j || !s->cand) {
+      !s->slot_stamp || !s->where || !s->seen || !s->seen_j || !s->serial || !s->cand) {
     or_destroy(s);
     return NULL;
   }
@@ -92,7 +102,8 @@ or_state* or_create(int32_t R, int32_t L, int32_t K, int32_t B, int32_t P,
       size_t n = (size_t)(ctx_cap[r] > 0 ? ctx_cap[r] : 1);
       s->where[u] = (int32_t*)malloc(sizeof(int32_t) * n);
       s->seen[u] = (int32_t*)calloc(n, sizeof(int32_t));
-      if (!s->where[u] || !s->seen[u]) {
+      s->seen_j[u] = (int32_t*)calloc(n, sizeof(int32_t));
+      if (!s->where[u] || !s->seen[u] || !s->seen_j[u]) {
         or_destroy(s);
         return NULL;
       }
@@ -107,9 +118,11 @@ void or_destroy(or_state* s) {
     for (int64_t u = 0; u < (int64_t)s->L * s->R; ++u) free(s->where[u]);
   if (s->seen)
     for (int64_t u = 0; u < (int64_t)s->L * s->R; ++u) free(s->seen[u]);
-  free(s->where); free(s->seen); free(s->serial);
+  if (s->seen_j)
+    for (int64_t u = 0; u < (int64_t)s->L * s->R; ++u) free(s->seen_j[u]);
+  free(s->where); free(s->seen); free(s->seen_j); free(s->serial);
   free(s->ctx); free(s->ctx_cap); free(s->page_table); free(s->hot_block);
-  free(s->slot_pos); free(s->slot_stamp); free(s->miss_j); free(s->cand);
+  free(s->slot_pos); free(s->slot_stamp); free(s->cand);
   free(s);
 }
 
@@ -176,27 +189,43 @@ static void sort_candidates(int32_t* cand, int32_t n, const int32_t* stamp) {
   free(tmp);
 }
 
-int32_t or_resolve(or_state* s, int32_t layer, int32_t req, const int32_t* topk,
-                   int32_t step, int32_t* out_row, int32_t* miss_log,
-                   int32_t* n_miss) {
-  if (layer < 0 || layer >= s->L || req < 0 || req >= s->R) return -1;
+int32_t or_resolve_tokens(or_state* s, int32_t layer, int32_t req, int32_t T,
+                          const int32_t* topk, int32_t step, int32_t* out_row,
+                          int32_t* miss_log, int32_t* n_miss) {
+  if (layer < 0 || layer >= s->L || req < 0 || req >= s->R || T <= 0) return -1;
   const int64_t u = unit_index(s, layer, req);
   int32_t* pos_of = s->slot_pos + u * s->B;
   int32_t* stamp = s->slot_stamp + u * s->B;
   int32_t* where = s->where[u];
   int32_t* seen = s->seen[u];
+  int32_t* seen_j = s->seen_j[u];
   const int32_t ctx = s->ctx[req];
   const int32_t call = ++s->serial[u];
-  int32_t err = 0, misses = 0;
+  const int32_t n = T * s->K;  /* the list: token t's row is entries t*K .. t*K+K-1 */
+  int32_t err = 0, misses = 0, n_alias = 0;
+  int32_t* miss_j = (int32_t*)malloc(sizeof(int32_t) * (size_t)n);
+  int32_t* alias = (int32_t*)malloc(sizeof(int32_t) * 2 * (size_t)n);  /* (j, first j) */
+  if (!miss_j || !alias) {
+    free(miss_j);
+    free(alias);
+    return -1;
+  }
 
-  /* Phase 1: classify every selection; refresh hits. */
-  for (int32_t j = 0; j < s->K; ++j) {
+  /* Phase 1: classify every entry; refresh hits. */
+  for (int32_t j = 0; j < n; ++j) {
     const int32_t p = topk[j];
     out_row[j] = -1;
     if (p == -1) continue;                       /* padding */
     if (p < 0 || p >= ctx) { err |= OR_ERR_RANGE; continue; }
-    if (seen[p] == call) { err |= OR_ERR_DUPLICATE; continue; }
+    if (seen[p] == call) {                       /* selected earlier in the list */
+      if (seen_j[p] / s->K == j / s->K) { err |= OR_ERR_DUPLICATE; continue; }
+      alias[2 * n_alias] = j;                    /* another token's: share its row */
+      alias[2 * n_alias + 1] = seen_j[p];
+      ++n_alias;
+      continue;
+    }
     seen[p] = call;
+    seen_j[p] = j;
     const int32_t blk = s->page_table[(int64_t)req * s->max_pages + p / s->P];
     if (blk >= 0) {                               /* resident: read in place */
       if (blk >= s->blocks_per_layer) { err |= OR_ERR_BLOCK; continue; }
@@ -209,7 +238,7 @@ int32_t or_resolve(or_state* s, int32_t layer, int32_t req, const int32_t* topk,
       out_row[j] = hot_row(s, req, slot);
       continue;
     }
-    s->miss_j[misses++] = j;                      /* host only: a miss */
+    miss_j[misses++] = j;                         /* host only: a miss */
   }
 
   /* Phase 2: victims are slots not used in this step, least recent first. */
@@ -220,7 +249,7 @@ int32_t or_resolve(or_state* s, int32_t layer, int32_t req, const int32_t* topk,
 
   int32_t served = 0;
   for (int32_t i = 0; i < misses; ++i) {
-    const int32_t j = s->miss_j[i], p = topk[j];
+    const int32_t j = miss_j[i], p = topk[j];
     if (i >= ncand) { err |= OR_ERR_CAPACITY; continue; }
     const int32_t slot = s->cand[i];
     if (pos_of[slot] >= 0) where[pos_of[slot]] = -1;   /* evict */
@@ -235,8 +264,18 @@ int32_t or_resolve(or_state* s, int32_t layer, int32_t req, const int32_t* topk,
     }
     ++served;
   }
+  /* Phase 3: repeats in later tokens take their first occurrence's row. */
+  for (int32_t i = 0; i < n_alias; ++i) out_row[alias[2 * i]] = out_row[alias[2 * i + 1]];
+  free(miss_j);
+  free(alias);
   if (n_miss) *n_miss = served;
   return err;
+}
+
+int32_t or_resolve(or_state* s, int32_t layer, int32_t req, const int32_t* topk,
+                   int32_t step, int32_t* out_row, int32_t* miss_log,
+                   int32_t* n_miss) {
+  return or_resolve_tokens(s, layer, req, 1, topk, step, out_row, miss_log, n_miss);
 }
 
 int32_t or_get_unit(const or_state* s, int32_t layer, int32_t req,

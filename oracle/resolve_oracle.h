@@ -33,6 +33,13 @@ int32_t or_set_hot_block(or_state* s, int32_t req, int32_t index, int32_t block)
 int32_t or_resolve(or_state* s, int32_t layer, int32_t req, const int32_t* topk,
                    int32_t step, int32_t* out_row, int32_t* miss_log,
                    int32_t* n_miss);
+/* Speculative decoding: one step of one unit for T verify tokens at once.
+ * topk[T*K] is token after token; out_row[T*K], miss_log[T*K][3].  A position
+ * an earlier token selected shares that entry's row; a repeat within one
+ * token's row is an input error. */
+int32_t or_resolve_tokens(or_state* s, int32_t layer, int32_t req, int32_t T,
+                          const int32_t* topk, int32_t step, int32_t* out_row,
+                          int32_t* miss_log, int32_t* n_miss);
 int32_t or_get_unit(const or_state* s, int32_t layer, int32_t req,
                     int32_t* slot_pos, int32_t* slot_stamp);
 int32_t or_row_content(const or_state* s, int32_t layer, int32_t req,

@@ -346,3 +346,119 @@ def test_attention_through_cache_equals_full_kv():
             via = synth.rows_at(w.seed, 0, 0, held)
             b, lb = oracle.sparse_mla_decode(q, via, None, W.SCALE)
             assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+# ------------------------------------------------ speculative decoding (T verify tokens)
+
+def test_tokens_hand_worked_example():
+    """B = 3 one-row slots (rows 20, 21, 22), K = 2, T = 2 verify tokens,
+    positions a=0, b=1, c=2, d=3.
+    Step 0, tokens [a b] [b c]: a, b, c miss and fill slots 0, 1, 2; token 1's
+    b shares token 0's row 21.
+    Step 1, tokens [c d] [a d]: c (slot 2) and a (slot 0) are hits, pinned for
+    the whole step; d misses and takes the only unpinned slot, 1 (b's);
+    token 1's d shares that row.  Resolving the tokens one call at a time
+    instead would let token 0's d evict a (slot 0, the lowest of the two
+    oldest), which token 1 then misses."""
+    o = _oracle_for(4, 1, 2, 3, [20, 21, 22], {})
+    rows, log, err = o.resolve_tokens(0, 0, np.array([[0, 1], [1, 2]]), 0)
+    assert err == 0 and rows.tolist() == [[20, 21], [21, 22]] and len(log) == 3
+    rows, log, err = o.resolve_tokens(0, 0, np.array([[2, 3], [0, 3]]), 1)
+    assert err == 0 and rows.tolist() == [[22, 21], [20, 21]]
+    assert log.tolist() == [[1, 3, 1]]  # (list index j, position, slot)
+    assert o.unit_state(0, 0)[0].tolist() == [0, 3, 2]
+    # the same two steps token by token give a different (worse) result
+    o2 = _oracle_for(4, 1, 2, 3, [20, 21, 22], {})
+    o2.resolve(0, 0, np.array([0, 1]), 0)
+    o2.resolve(0, 0, np.array([1, 2]), 0)
+    r0, l0, _ = o2.resolve(0, 0, np.array([2, 3]), 1)
+    r1, l1, _ = o2.resolve(0, 0, np.array([0, 3]), 1)
+    assert r0.tolist() == [22, 20] and r1.tolist() == [21, 20] and len(l0) + len(l1) == 2
+
+
+def _random_tokens_case(rng):
+    P = rng.choice([1, 2])
+    ctx = rng.randint(2, 8)
+    K = rng.randint(1, 3)
+    T = rng.randint(1, 3)
+    lo = max(1, (T * K + P - 1) // P) if rng.random() < 0.8 else 1
+    B = P * rng.randint(lo, max(lo, 9 // P))
+    n_pages = (ctx + P - 1) // P
+    resident = {pg: 10 + pg for pg in range(n_pages) if rng.random() < 0.25}
+    hot = [20 + i for i in range(B // P)]
+    steps = []
+    for _ in range(rng.randint(1, 4)):
+        toks = []
+        for _t in range(T):
+            sel = rng.sample(range(ctx), min(K, ctx))
+            sel += [-1] * (K - len(sel))
+            if rng.random() < 0.08:
+                sel[rng.randrange(K)] = rng.choice([ctx, ctx + 3, -2])  # invalid
+            if K > 1 and rng.random() < 0.08:
+                sel[1] = sel[0]                                        # repeat in a token
+            toks.append(sel)
+        steps.append(toks)
+    return ctx, P, K, T, B, hot, resident, steps
+
+
+def test_tokens_bruteforce_against_independent_lru():
+    """Thousands of tiny multi-token traces (ctx <= 8, K <= 3, T <= 3, B <= 9):
+    the oracle and the recency-list model agree on every row id, every slot's
+    position and every error bit."""
+    rng = random.Random(17)
+    for _ in range(3000):
+        ctx, P, K, T, B, hot, resident, steps = _random_tokens_case(rng)
+        o = _oracle_for(ctx, P, K, B, hot, resident)
+        ref = lru_alt.replay_tokens(ctx, P, B, hot, resident, steps)
+        for t, (toks, (rows_ref, holder_ref, err_ref)) in enumerate(zip(steps, ref)):
+            rows, _, err = o.resolve_tokens(0, 0, np.array(toks), t)
+            pos, _ = o.unit_state(0, 0)
+            assert rows.tolist() == rows_ref, (ctx, P, K, T, B, resident, steps, t)
+            assert pos.tolist() == holder_ref, (ctx, P, K, T, B, resident, steps, t)
+            assert err == err_ref
+
+
+def test_tokens_one_token_is_the_plain_call():
+    rng = random.Random(23)
+    for _ in range(500):
+        ctx, P, K, B, hot, resident, steps = _random_case(rng)
+        a = _oracle_for(ctx, P, K, B, hot, resident)
+        b = _oracle_for(ctx, P, K, B, hot, resident)
+        for t, sel in enumerate(steps):
+            ra, la, ea = a.resolve(0, 0, np.array(sel), t)
+            rb, lb, eb = b.resolve_tokens(0, 0, np.array([sel]), t)
+            assert rb[0].tolist() == ra.tolist() and lb.tolist() == la.tolist() and ea == eb
+
+
+def test_tokens_exactness_and_shared_rows():
+    """K 64, T 3 overlapping verify tokens, B = (T + 2) K: every entry's row
+    holds its position, a position shared by tokens has one row, and the misses
+    of a step are exactly the union's positions not yet in the buffer."""
+    rng = np.random.default_rng(29)
+    ctx, K, T, P = 2048, 64, 3, 64
+    B = (T + 2) * K
+    o = oracle.ResolveOracle(1, 1, K, B, P, [ctx], B // P)
+    o.set_ctx(0, ctx)
+    for i in range(B // P):
+        o.set_hot_block(0, i, i)
+    held = set()
+    prev = rng.choice(ctx, K, replace=False)
+    for t in range(20):
+        toks = []
+        for _ in range(T):
+            keep = rng.choice(prev, int(0.7 * K), replace=False)
+            rest = rng.choice(np.setdiff1d(np.arange(ctx), keep), K - len(keep), replace=False)
+            toks.append(rng.permutation(np.concatenate([keep, rest])))
+        rows, log, err = o.resolve_tokens(0, 0, np.array(toks), t)
+        assert err == 0
+        union = set(int(p) for tok in toks for p in tok)
+        assert len(log) == len(union - held)
+        seen = {}
+        for ti in range(T):
+            for j in range(K):
+                p, row = int(toks[ti][j]), int(rows[ti, j])
+                assert o.row_content(0, 0, row) == p
+                assert seen.setdefault(p, row) == row
+        pos, _ = o.unit_state(0, 0)
+        held = set(int(x) for x in pos if x >= 0)
+        prev = toks[-1]
