@@ -50,11 +50,11 @@ def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default 2000; the mixed workload: 120)")
+                    help="timed steps (default 2000; the mixed workload: 120; spec: 200)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="attention",
-                    choices=("attention", "resolve", "gather", "mixed"))
+                    choices=("attention", "resolve", "gather", "mixed", "spec"))
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--kernel-steps", type=int, default=500,
                     help="steps of the sequential per-kernel timing pass")
@@ -718,6 +718,135 @@ def run_mixed(args):
         dist.destroy_process_group()
 
 
+def run_spec(args):
+    """The speculative-decoding workload: the attention workload's 32 requests
+    x 2 layers (ctx 65536, K 2048) with T = 2 verify tokens per request and
+    step and B = (T + 2) K = 8192.  One step: per layer, hs_resolve_tokens (the
+    request's T rows as one list) then hs_sparse_mla_decode_tokens (one decode
+    per verify token), then the step counter.  Metric: resolved rows/s
+    (R x L x T x K per step); verify tokens/s alongside."""
+    import torch
+    import sparse_attention_kv_hs_gb300 as hs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    lib = hs.load()
+    steps_total = args.warmup + args.steps
+    w = W.make("spec", steps=steps_total)
+    w.req_base = replica_request_base(rank, w.R)
+    R, L, K, T, H = w.R, w.L, w.K, w.tokens, w.heads
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+    topk = np.empty((steps_total, L, R, T, K), dtype=np.int32)
+    with cf.ThreadPoolExecutor(max_workers=16) as ex:
+        def one(r):
+            topk[:, :, r] = w.trace_tokens(r)
+        list(ex.map(one, range(R)))
+    q = np.empty((Q_DISTINCT, L, R, T, H, W.ROW_ELEMS), dtype=np.uint16)
+    for t in range(Q_DISTINCT):
+        for l in range(L):
+            for r in range(R):
+                for k in range(T):
+                    q[t, l, r, k] = synth.q(w.seed, w.req_base + r, l, t * T + k, H)
+    scen = W.Scenario.build(w)
+    pool = make_pool(hs, w, scen)
+    topk_d = torch.from_numpy(topk).to(dev)
+    q_d = torch.from_numpy(q.view(np.int16)).to(dev)
+    rows_d = torch.empty((L, R, T, K), dtype=torch.int32, device=dev)
+    out_d = torch.empty((L, R, T, H, W.V_DIM), dtype=torch.bfloat16, device=dev)
+    lse_d = torch.empty((L, R, T, H), dtype=torch.float32, device=dev)
+    cnt_d = torch.zeros((steps_total, L, R), dtype=torch.int32, device=dev)
+    ph, step_ptr = pool.handle, pool.step.data_ptr()
+
+    def one_step(t, ev=None):
+        for l in range(L):
+            if ev is not None:
+                ev[0][l].record(stream)
+            st = lib.hs_resolve_tokens(ph, l, 1, T, topk_d[t, l].data_ptr(), step_ptr,
+                                       rows_d[l].data_ptr(), cnt_d[t, l].data_ptr(), None, sptr)
+            if ev is not None:
+                ev[1][l].record(stream)
+            st |= lib.hs_sparse_mla_decode_tokens(ph, l, T, q_d[t % Q_DISTINCT, l].data_ptr(),
+                                                  rows_d[l].data_ptr(), H, W.V_DIM, W.SCALE,
+                                                  out_d[l].data_ptr(), lse_d[l].data_ptr(), sptr)
+            if ev is not None:
+                ev[2][l].record(stream)
+            if st != 0:
+                raise RuntimeError(f"libhs call failed at step {t}: {hs.status_string(st)}")
+        lib.hs_step_advance(step_ptr, sptr)
+
+    peaks = load_peaks()
+    h2d_peak = measure_h2d_peak(torch) if not args.profile else float("nan")
+    for t in range(args.warmup):
+        one_step(t)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = ClockSampler(local) if not args.profile else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(L)] for _ in range(3)]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(args.steps):
+        one_step(args.warmup + i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop() if clocks else None
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    if hs.hs_check_errors(ph):
+        raise RuntimeError("device error word set in the spec run")
+    n_launch = args.steps * L
+    res_s = sum(e[0][l].elapsed_time(e[1][l]) for e in evs for l in range(L)) * 1e-3 / n_launch
+    att_s = sum(e[1][l].elapsed_time(e[2][l]) for e in evs for l in range(L)) * 1e-3 / n_launch
+    misses = int(cnt_d[args.warmup:].sum().item())
+    miss_bytes = misses * W.ROW_BYTES / n_launch
+    n_rows = R * T  # decode rows of one attention launch
+    att_bytes = n_rows * (K * W.ROW_BYTES + H * W.ROW_ELEMS * 2 + H * W.V_DIM * 2 + K * 4)
+    resolve_roof = {
+        "kernel": "resolve_kernel (T = 2 verify tokens)", "bound": "host_link",
+        "achieved": miss_bytes / res_s / 1e9, "peak": h2d_peak, "unit": "GB/s",
+        "peak_source": "in-run pinned cudaMemcpyAsync H2D, 1 GiB, best of 10",
+        "frac": miss_bytes / res_s / 1e9 / h2d_peak, "traffic": None,
+        "avg_launch_us": res_s * 1e6, "miss_rows_per_launch": misses / n_launch,
+    }
+    att_roof = {
+        "kernel": "mla_decode_kernel (64 decode rows)", "bound": "hbm",
+        "achieved": att_bytes / att_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": att_bytes / att_s / 1e9 / peaks["hbm_gbs"], "traffic": None,
+        "avg_launch_us": att_s * 1e6,
+    }
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": weak_scaling_rate(R * L * T * K, args.steps, world, elapsed_ms),
+            "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator; no dataset)",
+            "config": {"workload": (f"spec: {R} requests x {L} sparse layers, ctx {int(w.ctx[0])}, "
+                                    f"top-K {K}, {T} verify tokens, B {w.B}, {H} heads"),
+                       "l2": "inputs larger than L2, no flush", "parallelism": f"replicas x{world}"},
+            "verify_tok_s": weak_scaling_rate(R * T, args.steps, world, elapsed_ms),
+            "miss_rows_per_step": misses / args.steps,
+            "roofline": resolve_roof if res_s >= att_s else att_roof,
+            "kernels": [resolve_roof, att_roof], "host_link_peak_gbs": h2d_peak, "peaks": peaks,
+            "e2e": None, "gpu_launches": args.steps * (2 * L + 1), "clocks": clock_info,
+        }
+        print(json.dumps(line))
+    pool.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world):
     """Same step through the C ABI with HOST inputs/outputs: each step copies its
     top-K rows and queries from pinned host memory and reads the attention
@@ -842,12 +971,15 @@ def main(argv=None):
                                     f"(resolve + gather + fp64 attention), {secs:.1f} s"}))
         return
     if args.steps is None:
-        args.steps = 120 if args.workload == "mixed" else 2000
+        args.steps = {"mixed": 120, "spec": 200}.get(args.workload, 2000)
     if args.impl == "reference":
         run_reference(args)
         return
     if args.workload == "mixed":
         run_mixed(args)
+        return
+    if args.workload == "spec":
+        run_spec(args)
         return
     run_ours(args)
 

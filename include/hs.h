@@ -168,6 +168,32 @@ hs_status hs_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
                      int32_t* out_row_ids, int32_t* miss_count,
                      int32_t* miss_log, void* stream);
 
+/* RESOLVE for the T verify tokens of a speculative-decoding step.  Page "GLM
+ * 5.3 Optimizations, Part 1", section "Composition with the rest of vLLM":
+ * speculative decoding works through a replayable per-step resolver plan and
+ * the verify steps share the request's hot state; section "Exploiting
+ * sparsity when needed" (note): the hot buffer must hold every verify token's
+ * selection at once, (num_speculative_tokens + 2) x top-K rows.  Each unit's
+ * T rows of K positions are resolved as one list, token after token, exactly
+ * as hs_resolve resolves one row, except that a position an earlier token of
+ * the list also selected takes no slot of its own: it gets that entry's row
+ * (resident, hot or a served miss; -1 if that miss found no slot).  So the
+ * whole list's hits are pinned before any miss takes a victim, which calling
+ * hs_resolve once per token would not do.  A repeat within one token's row is
+ * an input error (bit DUPLICATE), as in hs_resolve.  T = 1 is hs_resolve.
+ *   topk_idx     device int32 [num_layers][R][T][K]
+ *   out_row_ids  device int32 [num_layers][R][T][K]
+ *   miss_count   device int32 [num_layers][R] or NULL: misses served
+ *   miss_log     device int32 [num_layers][R][T*K][3] or NULL: (j, position,
+ *                slot) per served miss, j indexing the unit's T*K list
+ * Size limit: the unit's tables for T*K entries and B slots must fit one
+ * CTA's shared memory (e.g. T = 2 at K = 2048, B = 8192); otherwise
+ * HS_ERR_INVALID.  Async, graph-capturable, no allocation. */
+hs_status hs_resolve_tokens(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
+                            int32_t num_tokens, const int32_t* topk_idx,
+                            const int32_t* d_step, int32_t* out_row_ids,
+                            int32_t* miss_count, int32_t* miss_log, void* stream);
+
 /* Gather rows of one layer by row id ("one stride"): out_rows[i] =
  * kv_pool[layer][row_ids[i]] (row_elems bf16 each); row id -1 gives a zero
  * row.  row_ids: device int32 [n_rows]; out_rows: device bf16
@@ -234,6 +260,23 @@ hs_status hs_decode_step(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
                          int32_t v_dim, float scale, const int32_t* d_step,
                          int32_t* out_row_ids, void* out, float* lse,
                          int32_t* miss_count, void* stream, void* copy_stream);
+
+/* Sparse MLA decode attention of one layer for the T verify tokens of a
+ * speculative-decoding step: each (request, token) has its own query and its
+ * own K rows (hs_resolve_tokens' output), computed as hs_sparse_mla_decode
+ * computes one request.
+ *   q        device bf16 [R][T][num_heads][576]
+ *   row_ids  device int32 [R][T][K]
+ *   out      device bf16 [R][T][num_heads][512]
+ *   lse      device float [R][T][num_heads] or NULL
+ * The K splits are limited to what the pool's workspace holds for R*T rows;
+ * HS_ERR_INVALID if even the fewest the kernel needs do not fit, or R*T >
+ * 65535.  Async, graph-capturable; shares the pool's workspace with
+ * hs_sparse_mla_decode (calls on one pool must not overlap). */
+hs_status hs_sparse_mla_decode_tokens(hs_pool* pool, int32_t layer, int32_t num_tokens,
+                                      const void* q, const int32_t* row_ids,
+                                      int32_t num_heads, int32_t v_dim, float scale,
+                                      void* out, float* lse, void* stream);
 
 /* Allocation-free variant of hs_sparse_mla_decode (no counterpart on the
  * pages: it exists for callers that cannot allocate device memory when they

@@ -38,7 +38,8 @@ EXPORTED = (
     "hs_set_request", "hs_map_page", "hs_load_page", "hs_resolve", "hs_gather",
     "hs_sparse_mla_decode", "hs_offload_prefix", "hs_commit_offload",
     "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
-    "hs_sparse_mla_decode_noalloc", "hs_decode_step",
+    "hs_sparse_mla_decode_noalloc", "hs_decode_step", "hs_resolve_tokens",
+    "hs_sparse_mla_decode_tokens",
 )
 
 
@@ -103,6 +104,8 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_host_read": [p, i64, p, p],
         "hs_sparse_mla_decode_noalloc": [p, i64, p, p, i32, i32, i32, i32, f32, p, p, p],
         "hs_decode_step": [p, i32, i32, p, p, i32, i32, f32, p, p, p, p, p, p, p],
+        "hs_resolve_tokens": [p, i32, i32, i32, p, p, p, p, p, p],
+        "hs_sparse_mla_decode_tokens": [p, i32, i32, p, p, i32, i32, f32, p, p, p],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -200,6 +203,25 @@ def hs_resolve(pool: int, layer_begin: int, num_layers: int, topk_idx, d_step, o
     _check(load().hs_resolve(pool, layer_begin, num_layers, _addr(topk_idx), _addr(d_step),
                              _addr(out_row_ids), _addr(miss_count), _addr(miss_log),
                              _stream(stream)), "hs_resolve")
+
+
+def hs_resolve_tokens(pool: int, layer_begin: int, num_layers: int, num_tokens: int, topk_idx,
+                      d_step, out_row_ids, miss_count=None, miss_log=None, stream=None) -> None:
+    """RESOLVE of the T verify tokens of a speculative-decoding step, as one
+    list per unit (topk_idx / out_row_ids [num_layers][R][T][K])."""
+    _check(load().hs_resolve_tokens(pool, layer_begin, num_layers, num_tokens, _addr(topk_idx),
+                                    _addr(d_step), _addr(out_row_ids), _addr(miss_count),
+                                    _addr(miss_log), _stream(stream)), "hs_resolve_tokens")
+
+
+def hs_sparse_mla_decode_tokens(pool: int, layer: int, num_tokens: int, q, row_ids,
+                                num_heads: int, v_dim: int, scale: float, out, lse=None,
+                                stream=None) -> None:
+    """Decode attention of the T verify tokens of each request (q [R][T][H][576],
+    row_ids [R][T][K], out [R][T][H][512])."""
+    _check(load().hs_sparse_mla_decode_tokens(pool, layer, num_tokens, _addr(q), _addr(row_ids),
+                                              num_heads, v_dim, scale, _addr(out), _addr(lse),
+                                              _stream(stream)), "hs_sparse_mla_decode_tokens")
 
 
 def hs_gather(pool: int, layer: int, row_ids, n_rows: int, out_rows, stream=None) -> None:

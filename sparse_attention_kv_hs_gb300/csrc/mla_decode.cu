@@ -1050,6 +1050,49 @@ extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void*
                              hs_stream(stream));
 }
 
+// Speculative decoding: each request's T verify tokens have their own query and
+// their own K rows (hs_resolve_tokens' output), so the T tokens of R requests
+// are R * T independent decode rows of the same kernel.  Their K splits are
+// capped so that the partials fit the pool's workspace (R x its splits).
+extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int32_t num_tokens,
+                                                 const void* q, const int32_t* row_ids,
+                                                 int32_t num_heads, int32_t v_dim, float scale,
+                                                 void* out, float* lse, void* stream) {
+  if (!p || !q || !row_ids || !out || num_tokens <= 0) return HS_ERR_INVALID;
+  if (layer < 0 || layer >= p->d.num_layers || num_heads <= 0 || num_heads > kHeads ||
+      v_dim != kDV || p->d.row_elems != kD || !(scale > 0.f) || p->attn_max_splits < 1 ||
+      !p->attn_kv_maps)
+    return HS_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return HS_ERR_INVALID;
+  const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
+  const int64_t n = (int64_t)p->d.num_requests * num_tokens;  // decode rows
+  if (rows_in_layer > INT32_MAX || n > 65535) return HS_ERR_INVALID;
+  const int tiles = (p->d.top_k + kTile - 1) / kTile;
+  const int min_splits = (tiles * kTile + kMaxSplitRows - 1) / kMaxSplitRows;
+  int splits = choose_splits(p->num_sms, (int)n, p->d.top_k);
+  const int fit = p->attn_max_splits / num_tokens;  // partials the workspace holds per row
+  if (splits > 1 && splits > fit) splits = fit > min_splits ? fit : min_splits;
+  if (splits > 1 && n * splits > (int64_t)p->d.num_requests * p->attn_max_splits)
+    return HS_ERR_INVALID;  // K too long for this many rows in the workspace
+  AttnArgs a;
+  a.kv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p->kv_pool) +
+                                        (int64_t)layer * rows_in_layer * kD);
+  a.row_ids = row_ids;
+  a.out = static_cast<uint16_t*>(out);
+  a.lse = lse;
+  a.ws_o = p->attn_o;
+  a.ws_lse = p->attn_ml;
+  a.error_word = p->error_word;
+  a.rows_in_layer = (int32_t)rows_in_layer;
+  a.K = p->d.top_k;
+  a.H = num_heads;
+  a.splits = splits;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  return launch_decode(a, static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q, (int)n,
+                       hs_stream(stream));
+}
+
 // ---------------------------------------------------------------------------
 // Allocation-free variant of the decode call.
 //

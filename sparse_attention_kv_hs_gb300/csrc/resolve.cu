@@ -60,6 +60,9 @@ struct ResolveArgs {
   int64_t host_tokens;
   int64_t blocks_per_layer;
   int32_t layer_begin, R, K, B, P, max_pages, row_vec;
+  // K is the length of a unit's list: T verify tokens' rows of ktok entries
+  // each, token after token (T = 1 outside speculative decoding)
+  int32_t ktok;
   int32_t sel_bits, kpt, bpt;
   int32_t copy_ctas;  // C: CTAs (a cluster) per unit
   int32_t smem_bytes; // dynamic shared memory per CTA (tables + staging)
@@ -68,7 +71,7 @@ struct ResolveArgs {
 // Both layouts start with one mbarrier at offset 0, so each CTA of a cluster
 // can address its peers' barrier without knowing their layout.
 struct SmemPlan {
-  size_t bar, order, sel_key, sel_j, miss_j, miss_p, victim, hot, flag, warp, ptab, total;
+  size_t bar, order, sel_key, sel_j, miss_j, miss_p, victim, hot, flag, warp, ptab, alias, total;
 };
 
 constexpr int kMaxSmemPages = 4096;  // page-table rows up to this width are staged in smem
@@ -89,17 +92,20 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int sel_bits)
   s.flag = o;      o = align16(o + B);
   s.warp = o;      o = align16(o + sizeof(int32_t) * (kWarps + 8));
   s.ptab = o;      o = align16(o + sizeof(int32_t) * kMaxSmemPages);
+  s.alias = o;     o = align16(o + sizeof(uint32_t) * kThreads);
   s.total = o;
   return s;
 }
 
 // Fetch CTAs: their share's misses (j, position, destination row id), the
 // scan scratch, then staging for as many rows as fit.
+// With several verify tokens (dedup_bits > 0) a fetch CTA also holds its own
+// selection hash, so that a position several tokens select is fetched once.
 struct FetchPlan {
-  size_t bar, j, p, dst, warp, stage;
+  size_t bar, j, p, dst, warp, sel_key, sel_j, stage;
 };
 
-__host__ __device__ inline FetchPlan fetch_plan(int S) {
+__host__ __device__ inline FetchPlan fetch_plan(int S, int dedup_bits) {
   FetchPlan f;
   size_t o = 0;
   f.bar = o;   o = 16;
@@ -107,6 +113,9 @@ __host__ __device__ inline FetchPlan fetch_plan(int S) {
   f.p = o;     o = align16(o + sizeof(int32_t) * S);
   f.dst = o;   o = align16(o + sizeof(int32_t) * S);
   f.warp = o;  o = align16(o + sizeof(int32_t) * (kWarps + 8));
+  const size_t hash = dedup_bits > 0 ? sizeof(int32_t) * (size_t(1) << dedup_bits) : 0;
+  f.sel_key = o;  o = align16(o + hash);
+  f.sel_j = o;    o = align16(o + hash);
   f.stage = o;
   return f;
 }
@@ -138,6 +147,32 @@ __device__ __forceinline__ bool wait_peer_bar(uint32_t bar, uint32_t parity) {
 
 __device__ __forceinline__ uint32_t hash_pos(int32_t p, int bits) {
   return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits);
+}
+
+// Selection hash in shared memory (open addressing, linear probing; key -1 =
+// empty): position -> the smallest list index j that selects it.
+__device__ __forceinline__ void sel_insert(int32_t* key, int32_t* first, int bits, int32_t p,
+                                           int j) {
+  const int mask = (1 << bits) - 1;
+  uint32_t h = hash_pos(p, bits);
+  for (int probe = 0; probe <= mask; ++probe) {
+    const int32_t prev = atomicCAS(&key[h], -1, p);
+    if (prev == -1 || prev == p) {
+      atomicMin(&first[h], j);
+      return;
+    }
+    h = (h + 1) & mask;
+  }
+}
+__device__ __forceinline__ int32_t sel_first(const int32_t* key, const int32_t* first, int bits,
+                                             int32_t p) {
+  const int mask = (1 << bits) - 1;
+  uint32_t h = hash_pos(p, bits);
+  for (int probe = 0; probe <= mask; ++probe) {
+    if (key[h] == p) return first[h];
+    h = (h + 1) & mask;
+  }
+  return -1;
 }
 
 // Exclusive scan of one value per thread over the CTA; *total gets the sum.
@@ -291,15 +326,31 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     const int S = (K + F - 1) / F;
     const int j_lo = f * S, j_hi = min(K, j_lo + S);
     const int kptf = (S + kThreads - 1) / kThreads;  // <= kpt <= 8
-    const FetchPlan fp = fetch_plan(S);
+    const bool dedup = a.K != a.ktok;  // several verify tokens: fetch each position once
+    const FetchPlan fp = fetch_plan(S, dedup ? a.sel_bits : 0);
     int32_t* f_j = reinterpret_cast<int32_t*>(smem + fp.j);
     int32_t* f_p = reinterpret_cast<int32_t*>(smem + fp.p);
     int32_t* f_dst = reinterpret_cast<int32_t*>(smem + fp.dst);
     int* s_warp = reinterpret_cast<int*>(smem + fp.warp);
     const int cap = (int)((a.smem_bytes - (int64_t)fp.stage) / row_bytes);
 
+    int32_t* f_key = reinterpret_cast<int32_t*>(smem + fp.sel_key);
+    int32_t* f_first = reinterpret_cast<int32_t*>(smem + fp.sel_j);
+    if (dedup) {  // the whole list's selection hash, as CTA 0 builds it
+      for (int h = tid; h < (1 << a.sel_bits); h += kThreads) {
+        f_key[h] = -1;
+        f_first[h] = INT32_MAX;
+      }
+      __syncthreads();
+      for (int j = tid; j < K; j += kThreads) {
+        const int32_t p = topk[j];
+        if (p >= 0 && p < ctx) sel_insert(f_key, f_first, a.sel_bits, p, j);
+      }
+      __syncthreads();
+    }
+
     // classify this CTA's share: a miss is a valid position that is neither
-    // resident nor in the hot buffer
+    // resident nor in the hot buffer (with several tokens: at its first entry)
     const int j0 = j_lo + tid * kptf;
     int32_t my_p[8];
     uint32_t miss_mask = 0;
@@ -313,6 +364,11 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       if (p < 0 || p >= ctx) continue;
       if (ptab[p / P] >= 0) continue;
       if (inv_u[p] < 0) miss_mask |= 1u << q;
+    }
+    if (dedup) {  // a position an earlier entry selected is fetched for that entry only
+      for (int q = 0; q < kptf; ++q)  // (topk re-read: no array indexed at run time)
+        if ((miss_mask >> q) & 1u && sel_first(f_key, f_first, a.sel_bits, topk[j0 + q]) != j0 + q)
+          miss_mask &= ~(1u << q);
     }
     int n_local;
     int mi = block_exclusive_scan(__popc(miss_mask), s_warp, &n_local);
@@ -358,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   uint8_t* s_flag = smem + sp.flag;
   int* s_warp = reinterpret_cast<int*>(smem + sp.warp);
   int32_t* s_ptab = reinterpret_cast<int32_t*>(smem + sp.ptab);
+  uint32_t* s_alias = reinterpret_cast<uint32_t*>(smem + sp.alias);
   int* s_err = s_warp + kWarps;
   const int hot_per_req = B / P;
   const int sel_mask = (1 << a.sel_bits) - 1;
@@ -393,20 +450,13 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     my_p[q] = (q < a.kpt && j < K) ? topk[j] : -1;
     const int32_t p = my_p[q];
     if (q >= a.kpt || j >= K || p < 0 || p >= ctx) continue;
-    uint32_t h = hash_pos(p, a.sel_bits);
-    for (int probe = 0; probe <= sel_mask; ++probe) {
-      const int32_t prev = atomicCAS(&s_sel_key[h], -1, p);
-      if (prev == -1 || prev == p) {
-        atomicMin(&s_sel_j[h], j);
-        break;
-      }
-      h = (h + 1) & sel_mask;
-    }
+    sel_insert(s_sel_key, s_sel_j, a.sel_bits, p, j);
   }
   __syncthreads();
 
   // ---- 2. classify; refresh hits ----------------------------------------
   uint32_t miss_mask = 0;
+  uint32_t alias_mask = 0;  // repeats of a position an earlier verify token selected
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int j = j0 + q;
@@ -422,19 +472,15 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       out[j] = -1;
       continue;
     }
-    {  // first occurrence of p in this row?
-      uint32_t h = hash_pos(p, a.sel_bits);
-      int32_t first = -1;
-      for (int probe = 0; probe <= sel_mask; ++probe) {
-        if (s_sel_key[h] == p) {
-          first = s_sel_j[h];
-          break;
-        }
-        h = (h + 1) & sel_mask;
-      }
+    {  // first occurrence of p in the list?
+      const int32_t first = sel_first(s_sel_key, s_sel_j, a.sel_bits, p);
       if (first != j) {
-        err |= HS_DEV_ERR_DUPLICATE;
-        out[j] = -1;
+        if (first / a.ktok == j / a.ktok) {  // a repeat within one token's row
+          err |= HS_DEV_ERR_DUPLICATE;
+          out[j] = -1;
+        } else {  // another token's position: its row, once served (below)
+          alias_mask |= 1u << q;
+        }
         continue;
       }
     }
@@ -458,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     }
   }
 
+  s_alias[tid] = alias_mask;  // read back once the misses are served
   // misses numbered in selection (j) order
   int n_miss_total;
   const int my_misses = __popc(miss_mask);
@@ -556,6 +603,14 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   if (err) atomicOr(s_err, err);
   __syncthreads();
   if (tid == 0 && *s_err) atomicOr(a.error_word, *s_err);
+  if (const uint32_t alias_mask = s_alias[tid]) {  // a later token's repeat: its first entry's row
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (alias_mask & (1u << q)) {
+        const int j = j0 + q;
+        out[j] = __ldcg(out + sel_first(s_sel_key, s_sel_j, a.sel_bits, topk[j]));
+      }
+  }
 
   if (C > 1) {  // (2) every miss's row id is written
     if (tid == 0)
@@ -591,7 +646,7 @@ hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes, int max_
   int dev = 0, optin = 0;
   HS_CUDA_TRY(cudaGetDevice(&dev));
   HS_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-  if (tables > (size_t)optin || fetch_plan(K).stage > (size_t)optin)
+  if (tables > (size_t)optin || fetch_plan(K, 0).stage > (size_t)optin)
     return HS_ERR_INVALID;  // K and B too large for one CTA
   // One CTA per SM either way (1024 threads): what the tables leave is staging.
   const size_t smem = (size_t)optin;
@@ -629,10 +684,14 @@ hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes, int max_
   return HS_OK;
 }
 
-hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
-                            const int32_t* topk, const int32_t* d_step, int32_t* out_rows,
-                            int32_t* miss_count, int32_t* miss_log, int max_cluster,
-                            cudaStream_t stream) {
+namespace {
+
+// RESOLVE of `num_tokens` verify tokens per unit (1 outside speculative
+// decoding): the unit's list is their num_tokens * K entries, token after token.
+hs_status launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers, int32_t num_tokens,
+                         const int32_t* topk, const int32_t* d_step, int32_t* out_rows,
+                         int32_t* miss_count, int32_t* miss_log, int max_cluster,
+                         cudaStream_t stream) {
   ResolveArgs a;
   a.topk = topk;
   a.d_step = d_step;
@@ -654,7 +713,8 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
   a.blocks_per_layer = p->blocks_per_layer;
   a.layer_begin = layer_begin;
   a.R = p->d.num_requests;
-  a.K = p->d.top_k;
+  a.ktok = p->d.top_k;
+  a.K = num_tokens * p->d.top_k;
   a.B = p->d.hot_slots;
   a.P = p->d.page_tokens;
   a.max_pages = p->d.max_pages;
@@ -666,6 +726,9 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
   // The kernel's dynamic shared-memory limit was raised by hs_pool_create
   // (hs_resolve_configure): nothing here may call outside the stream.
   const size_t smem = p->resolve_smem;
+  if (num_tokens > 1 && (smem_plan(a.K, a.B, a.P, a.sel_bits).total > smem ||
+                         fetch_plan(a.K, a.sel_bits).stage > smem))
+    return HS_ERR_INVALID;  // the list's tables do not fit one CTA's shared memory
   a.smem_bytes = (int32_t)smem;
   // CTAs per unit: the largest cluster size (8, 4, 2) whose clusters, one per
   // unit, all run at once; else one CTA per unit
@@ -697,6 +760,16 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
   return HS_OK;
 }
 
+}  // namespace
+
+hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
+                            const int32_t* topk, const int32_t* d_step, int32_t* out_rows,
+                            int32_t* miss_count, int32_t* miss_log, int max_cluster,
+                            cudaStream_t stream) {
+  return launch_resolve(p, layer_begin, num_layers, 1, topk, d_step, out_rows, miss_count,
+                        miss_log, max_cluster, stream);
+}
+
 extern "C" hs_status hs_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
                                 const int32_t* topk_idx, const int32_t* d_step,
                                 int32_t* out_row_ids, int32_t* miss_count, int32_t* miss_log,
@@ -706,4 +779,15 @@ extern "C" hs_status hs_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_
     return HS_ERR_INVALID;
   return hs_launch_resolve(pool, layer_begin, num_layers, topk_idx, d_step, out_row_ids,
                            miss_count, miss_log, 0, hs_stream(stream));
+}
+
+extern "C" hs_status hs_resolve_tokens(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
+                                       int32_t num_tokens, const int32_t* topk_idx,
+                                       const int32_t* d_step, int32_t* out_row_ids,
+                                       int32_t* miss_count, int32_t* miss_log, void* stream) {
+  if (!pool || !topk_idx || !d_step || !out_row_ids || num_tokens <= 0) return HS_ERR_INVALID;
+  if (num_layers <= 0 || layer_begin < 0 || layer_begin + num_layers > pool->d.num_layers)
+    return HS_ERR_INVALID;
+  return launch_resolve(pool, layer_begin, num_layers, num_tokens, topk_idx, d_step, out_row_ids,
+                        miss_count, miss_log, 0, hs_stream(stream));
 }

@@ -18,6 +18,10 @@ Workloads (sizes as stated for the HiSparse decode path):
             K 2048, B 4096, tail 4096; 1/4 zero residency, 1/4 fully resident,
             1/2 resident tail; 5% of requests append a 256-token page per step
             (queued for host offload); 128 steps, 70/20/10 drift
+  spec      the attention workload with speculative decoding: T = 2 verify
+            tokens per request and step (one speculative token), B = (T + 2) K
+            = 8192; token 0 drifts as in "attention", token t > 0 keeps 85% of
+            token t-1's selection and draws the rest uniformly
 """
 from __future__ import annotations
 
@@ -35,6 +39,7 @@ V_DIM = 512
 SCALE = 1.0 / math.sqrt(192.0)
 
 TAG_SCEN = 0x5343454E  # "SCEN"
+TAG_SPEC = 0x53504543  # "SPEC"
 
 
 @dataclasses.dataclass
@@ -57,6 +62,8 @@ class Workload:
     P: int = PAGE_TOKENS
     zipf_s: float = 1.1
     req_base: int = 0               # generator id of request 0 (replicas use disjoint ids)
+    tokens: int = 1                 # verify tokens per step (speculative decoding)
+    token_share: float = 0.0        # share of token t-1's selection token t keeps
 
     # ---- derived scenario -------------------------------------------------
     def append_schedule(self) -> list:
@@ -130,6 +137,40 @@ class Workload:
                       self.ctx_per_step()[:, r].astype(np.int32), self.reuse,
                       self.zipf_frac, self.zipf_s, self.layer_share)
 
+    def trace_tokens(self, r: int) -> np.ndarray:
+        """[steps, L, T, K] selections of request r's T verify tokens: token 0
+        is trace(r); token t > 0 keeps floor(token_share * K) positions of
+        token t-1's selection (a seeded choice) and draws the rest uniformly
+        over the context, never repeating a position within the token."""
+        base = self.trace(r)
+        steps, L, K = base.shape
+        out = np.empty((steps, L, self.tokens, K), dtype=np.int32)
+        out[:, :, 0, :] = base
+        keep = int(self.token_share * K)
+        ctx = self.ctx_per_step()[:, r]
+        for t in range(steps):
+            n = int(ctx[t])
+            for l in range(L):
+                for tok in range(1, self.tokens):
+                    g = np.random.Generator(np.random.PCG64(
+                        _key(self.seed, TAG_SPEC, self.req_base + r, t * L + l, tok)))
+                    prev = out[t, l, tok - 1]
+                    kept = g.choice(prev, keep, replace=False)
+                    taken = np.zeros(n, dtype=bool)
+                    taken[kept] = True
+                    fresh = []
+                    while len(fresh) < K - keep:
+                        cand = g.integers(0, n, size=2 * (K - keep))
+                        for c in cand:
+                            if not taken[c]:
+                                taken[c] = True
+                                fresh.append(c)
+                                if len(fresh) == K - keep:
+                                    break
+                    row = np.concatenate([kept, np.array(fresh, dtype=np.int64)])
+                    out[t, l, tok] = g.permutation(row)
+        return out
+
     def host_bytes(self) -> int:
         return self.host_tokens() * self.L * ROW_BYTES
 
@@ -188,6 +229,12 @@ def make(name: str, *, R: int | None = None, steps: int | None = None,
         w = Workload("attention", R_, L or 2, 2048, 4096, steps or 64,
                      np.full(R_, ctx or 65536, dtype=np.int64), 0, ["zero"] * R_,
                      0.7, 0.0, 0.0, 128, 1004)
+    elif name == "spec":
+        R_ = R or 32
+        T = 2
+        w = Workload("spec", R_, L or 2, 2048, (T + 2) * 2048, steps or 64,
+                     np.full(R_, ctx or 65536, dtype=np.int64), 0, ["zero"] * R_,
+                     0.7, 0.0, 0.0, 128, 1006, tokens=T, token_share=0.85)
     elif name == "mixed":
         R_ = R or 128
         steps_ = steps or 128
@@ -203,7 +250,7 @@ def make(name: str, *, R: int | None = None, steps: int | None = None,
     return w
 
 
-NAMES = ("tiny", "resolve", "gather", "attention", "mixed")
+NAMES = ("tiny", "resolve", "gather", "attention", "mixed", "spec")
 
 
 @dataclasses.dataclass
