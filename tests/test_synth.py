@@ -72,3 +72,23 @@ def test_mixed_workload_scenario_is_consistent():
         assert len(set(live.values())) == len(live)
         assert all(b < s.blocks_per_layer for b in live.values())
         assert all(b >= w.R * w.hot_blocks_per_request() for b in live.values())
+
+
+def test_spec_token_traces():
+    """Verify-token traces: token 0 is the plain trace; token t > 0 keeps
+    floor(0.85 K) of token t-1's positions, never repeats one within a token,
+    stays inside the context, and is reproducible."""
+    w = W.make("spec", R=2, steps=5)
+    for r in range(2):
+        tt = w.trace_tokens(r)
+        assert tt.shape == (5, w.L, w.tokens, w.K)
+        np.testing.assert_array_equal(tt[:, :, 0], w.trace(r))
+        keep = int(w.token_share * w.K)
+        for t in range(5):
+            for l in range(w.L):
+                for k in range(1, w.tokens):
+                    row, prev = tt[t, l, k], tt[t, l, k - 1]
+                    assert len(set(row.tolist())) == w.K
+                    assert row.min() >= 0 and row.max() < int(w.ctx[r])
+                    assert len(set(row.tolist()) & set(prev.tolist())) >= keep
+        np.testing.assert_array_equal(tt, w.trace_tokens(r))
