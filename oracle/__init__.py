@@ -15,6 +15,9 @@ with the CUDA library (``sparse_attention_kv_hs_gb300``) and never imports it.
   Belady replacement with RESOLVE's step structure (C, policy_sim.c), for the
   replacement-policy comparison of page "59188saintaubert.com ... HiSparse",
   section 04.
+* ``fp8_rows_to_f64`` -- the rows an FP8 KV row (656 bytes: E4M3 latent codes,
+  per-128 fp32 scales, bf16 rope) stands for, decoded from the E4M3
+  definition.
 * ``sparse_mla_decode`` -- attention of one decode query over exactly the K
   selected rows, in fp64 (softmax(scale * q k^T) v with v = the first 512
   columns of each 576-wide latent row).  The pages state the method is exact:
@@ -194,6 +197,34 @@ def policy_misses(policy: str, trace, hot_slots: int, ctx: int, seed: int = 0) -
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """Exact bf16 -> float64 decoding (bf16 bits are the top half of an fp32)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an OCP FP8 E4M3 code: 1 sign bit, 4 exponent bits (bias 7), 3
+    mantissa bits; exponent field 0 is subnormal (m/8 * 2^-6); S.1111.111 is
+    NaN and there are no infinities (largest finite 448)."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def fp8_rows_to_f64(raw: np.ndarray) -> np.ndarray:
+    """FP8 KV rows ([n, 656] bytes: 512 E4M3 latent codes, 4 fp32 group scales,
+    64 bf16 rope values) -> the 576-wide rows they stand for, exactly, in fp64:
+    latent value i = E4M3(code i) * scale[i // 128]."""
+    raw = np.ascontiguousarray(raw, dtype=np.uint8).reshape(-1, 656)
+    lat = E4M3_TABLE[raw[:, :512]]
+    scales = raw[:, 512:528].copy().view(np.float32).astype(np.float64)   # [n, 4]
+    lat = lat * np.repeat(scales, 128, axis=1)
+    rope = bf16_bits_to_f64(raw[:, 528:656].copy().view(np.uint16))
+    return np.concatenate([lat, rope], axis=1)
 
 
 def sparse_mla_decode(q: np.ndarray, rows: np.ndarray, valid: np.ndarray | None,

@@ -57,6 +57,12 @@ def _load():
             lib.sy_fill_rows.argtypes = [u64, i32, i32, i64, i64, i32, p, i32]
             lib.sy_fill_rows_at.restype = None
             lib.sy_fill_rows_at.argtypes = [u64, i32, i32, p, i64, i32, p]
+            lib.sy_fill_rows_fp8.restype = None
+            lib.sy_fill_rows_fp8.argtypes = [u64, i32, i32, i64, i64, p, i32]
+            lib.sy_fill_rows_fp8_at.restype = None
+            lib.sy_fill_rows_fp8_at.argtypes = [u64, i32, i32, p, i64, p]
+            lib.sy_e4m3_encode.restype = ctypes.c_uint8
+            lib.sy_e4m3_encode.argtypes = [ctypes.c_float]
             lib.sy_fill_q.restype = None
             lib.sy_fill_q.argtypes = [u64, i32, i32, i32, i32, i32, p]
             lib.sy_trace_request.restype = i32
@@ -118,6 +124,38 @@ def rows_at(seed: int, req: int, layer: int, pos, width: int = ROW_ELEMS) -> np.
     out = np.empty((pos.size, width), dtype=np.uint16)
     _load().sy_fill_rows_at(seed, req, layer, pos.ctypes.data, pos.size, width, out.ctypes.data)
     return out
+
+
+FP8_ROW_BYTES = 656
+
+
+def rows_fp8(seed: int, req: int, layer: int, pos0: int, n: int, threads: int = 1,
+             out: np.ndarray | None = None) -> np.ndarray:
+    """The KV rows of rows(...) stored as 656-byte FP8 rows (synth.h), [n, 656] uint8."""
+    if out is None:
+        out = np.empty((n, FP8_ROW_BYTES), dtype=np.uint8)
+    assert out.dtype == np.uint8 and out.flags.c_contiguous and out.size >= n * FP8_ROW_BYTES
+    _load().sy_fill_rows_fp8(seed, req, layer, pos0, n, out.ctypes.data, threads)
+    return out
+
+
+def rows_fp8_into(seed: int, req: int, layer: int, pos0: int, n: int, addr: int,
+                  threads: int) -> None:
+    """FP8 rows straight to a raw host address (e.g. a pinned pool)."""
+    _load().sy_fill_rows_fp8(seed, req, layer, pos0, n, ctypes.c_void_p(addr), threads)
+
+
+def rows_fp8_at(seed: int, req: int, layer: int, pos) -> np.ndarray:
+    """FP8 rows for an explicit position list (negative position -> zero row)."""
+    pos = np.ascontiguousarray(pos, dtype=np.int32).reshape(-1)
+    out = np.empty((pos.size, FP8_ROW_BYTES), dtype=np.uint8)
+    _load().sy_fill_rows_fp8_at(seed, req, layer, pos.ctypes.data, pos.size, out.ctypes.data)
+    return out
+
+
+def e4m3_encode(v: float) -> int:
+    """The generator's fp32 -> E4M3 rounding (for its own tests)."""
+    return int(_load().sy_e4m3_encode(float(v)))
 
 
 def q(seed: int, req: int, layer: int, step: int, heads: int,

@@ -306,3 +306,113 @@ int32_t sy_trace_request(const sy_trace_params* prm, int32_t req,
   free(cur);
   return 0;
 }
+
+/* ---- FP8 rows (see synth.h) ------------------------------------------- */
+
+uint8_t sy_e4m3_encode(float v) {
+  const uint8_t sign = (v < 0.0f || (v == 0.0f && signbit(v))) ? 0x80u : 0u;
+  double a = fabs((double)v);
+  if (!(a < 448.0)) return (uint8_t)(sign | 0x7Eu); /* saturate (also NaN input) */
+  if (a < 0x1p-6) {                                  /* subnormal range: m * 2^-9 */
+    const double m = nearbyint(a * 512.0);          /* ties to even (default mode) */
+    if (m >= 8.0) return (uint8_t)(sign | 0x08u);   /* rounds up to 2^-6 */
+    return (uint8_t)(sign | (uint8_t)m);
+  }
+  int x;
+  const double f = frexp(a, &x);            /* a = f * 2^x, f in [0.5, 1) */
+  int e = x - 1;                            /* a = (2f) * 2^e, 2f in [1, 2) */
+  double q = nearbyint(2.0 * f * 8.0);      /* significand in eighths: 8 .. 16 */
+  if (q >= 16.0) {
+    q = 8.0;
+    ++e;
+  }
+  const int field = e + 7;
+  const int m = (int)q - 8;
+  if (field > 15 || (field == 15 && m == 7)) return (uint8_t)(sign | 0x7Eu);
+  return (uint8_t)(sign | (uint8_t)(field << 3) | (uint8_t)m);
+}
+
+static float bf16_to_float_(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static void quantize_row_fp8(const uint16_t* src, uint8_t* dst) {
+  for (int g = 0; g < 4; ++g) {
+    float mx = 0.0f;
+    for (int i = 0; i < 128; ++i) {
+      const float a = fabsf(bf16_to_float_(src[128 * g + i]));
+      if (a > mx) mx = a;
+    }
+    const float scale = mx > 0.0f ? mx / 448.0f : 1.0f;
+    memcpy(dst + 512 + 4 * g, &scale, 4);
+    for (int i = 0; i < 128; ++i) {
+      const float y = bf16_to_float_(src[128 * g + i]) / scale;
+      dst[128 * g + i] = sy_e4m3_encode(y);
+    }
+  }
+  memcpy(dst + 528, src + 512, 64 * sizeof(uint16_t)); /* rope stays bf16 */
+}
+
+static void fill_rows_fp8_serial(uint64_t seed, int32_t req, int32_t layer, int64_t pos0,
+                                 int64_t n, uint8_t* dst) {
+  uint16_t row[576];
+  for (int64_t i = 0; i < n; ++i) {
+    fill_rows_serial(seed, req, layer, pos0 + i, 1, 576, row);
+    quantize_row_fp8(row, dst + i * SY_FP8_ROW_BYTES);
+  }
+}
+
+typedef struct {
+  uint64_t seed;
+  int32_t req, layer;
+  int64_t pos0, n;
+  uint8_t* dst;
+} fill_fp8_job;
+
+static void* fill_fp8_worker(void* arg) {
+  fill_fp8_job* j = (fill_fp8_job*)arg;
+  fill_rows_fp8_serial(j->seed, j->req, j->layer, j->pos0, j->n, j->dst);
+  return NULL;
+}
+
+void sy_fill_rows_fp8(uint64_t seed, int32_t req, int32_t layer, int64_t pos0,
+                      int64_t n, uint8_t* dst, int32_t threads) {
+  if (n <= 0) return;
+  if (threads <= 1 || n < 4096) {
+    fill_rows_fp8_serial(seed, req, layer, pos0, n, dst);
+    return;
+  }
+  if (threads > 256) threads = 256;
+  pthread_t tid[256];
+  fill_fp8_job jobs[256];
+  int64_t per = (n + threads - 1) / threads;
+  int32_t started = 0;
+  for (int32_t t = 0; t < threads; ++t) {
+    int64_t a = (int64_t)t * per, b = a + per;
+    if (a >= n) break;
+    if (b > n) b = n;
+    jobs[t] = (fill_fp8_job){seed, req, layer, pos0 + a, b - a, dst + a * SY_FP8_ROW_BYTES};
+    if (pthread_create(&tid[t], NULL, fill_fp8_worker, &jobs[t]) != 0) {
+      fill_fp8_worker(&jobs[t]);
+      tid[t] = 0;
+    }
+    started = t + 1;
+  }
+  for (int32_t t = 0; t < started; ++t)
+    if (tid[t]) pthread_join(tid[t], NULL);
+}
+
+void sy_fill_rows_fp8_at(uint64_t seed, int32_t req, int32_t layer,
+                         const int32_t* pos, int64_t n, uint8_t* dst) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint8_t* o = dst + i * SY_FP8_ROW_BYTES;
+    if (pos[i] < 0) {
+      memset(o, 0, SY_FP8_ROW_BYTES);
+      continue;
+    }
+    fill_rows_fp8_serial(seed, req, layer, pos[i], 1, o);
+  }
+}

@@ -48,6 +48,22 @@ void sy_fill_rows_at(uint64_t seed, int32_t req, int32_t layer,
                      const int32_t* pos, int64_t n, int32_t width,
                      uint16_t* dst);
 
+/* The same rows (576 wide) stored as FP8 rows of 656 bytes: bytes 0..511 the
+ * 512 latent values as OCP E4M3 codes (bias 7, largest 448, no infinities),
+ * bytes 512..527 four fp32 scales (scale g multiplies latent values
+ * 128g .. 128g+127), bytes 528..655 the 64 rope values as bf16.  A group's
+ * scale is its largest magnitude / 448 (1 for an all-zero group); each latent
+ * value is divided by its scale in fp32 and rounded to the nearest E4M3 value
+ * (ties to even, magnitudes above 448 saturate to 448). */
+#define SY_FP8_ROW_BYTES 656
+void sy_fill_rows_fp8(uint64_t seed, int32_t req, int32_t layer, int64_t pos0,
+                      int64_t n, uint8_t* dst, int32_t threads);
+void sy_fill_rows_fp8_at(uint64_t seed, int32_t req, int32_t layer,
+                         const int32_t* pos, int64_t n, uint8_t* dst);
+/* One fp32 value -> its E4M3 code as above (round to nearest, ties to even,
+ * saturating at 448). */
+uint8_t sy_e4m3_encode(float v);
+
 /* Decode query of (seed, req, layer, step): heads x width bf16 values. */
 void sy_fill_q(uint64_t seed, int32_t req, int32_t layer, int32_t step,
                int32_t heads, int32_t width, uint16_t* dst);
