@@ -73,6 +73,16 @@ typedef enum {
                                   row) is not finite or has magnitude >= 65536; the P.V
                                   product runs in fp16 (see hs_sparse_mla_decode) */
 
+/* KV row formats.  HS_KV_BF16: row_elems bf16 values (2 * row_elems bytes).
+ * HS_KV_FP8 (row_elems must be 576): 656 bytes -- bytes 0..511 the 512 latent
+ * values as OCP FP8 E4M3 codes (bias 7, largest 448, no infinities), bytes
+ * 512..527 four fp32 scales (latent value i = E4M3(code i) * scale[i / 128]),
+ * bytes 528..655 the 64 rope values as bf16.  The pages' benchmark runs an FP8
+ * KV cache but gives no row layout; this is the one this library defines.
+ * RESOLVE, gather, page loads and offload move rows as opaque bytes in
+ * either format. */
+enum { HS_KV_BF16 = 0, HS_KV_FP8 = 1 };
+
 typedef struct {
   int32_t num_requests;    /* R */
   int32_t num_layers;      /* L sparse layers */
@@ -81,7 +91,7 @@ typedef struct {
   int32_t page_tokens;     /* P: tokens per page/block */
   int32_t row_elems;       /* bf16 values per KV row; multiple of 8 (576 here) */
   int32_t max_pages;       /* logical pages per request (page table width) */
-  int32_t reserved;        /* must be 0 */
+  int32_t kv_format;       /* HS_KV_BF16 or HS_KV_FP8 (see below) */
   int64_t host_tokens;     /* rows per layer in the pinned host pool */
   int64_t resident_blocks; /* blocks per layer for resident pages (beyond the hot buffers) */
 } hs_pool_desc;

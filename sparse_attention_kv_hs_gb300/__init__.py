@@ -25,6 +25,10 @@ HS_ERR_CAPACITY = -4
 HS_ERR_DEVICE = -5
 HS_ERR_TIMEOUT = -6
 
+HS_KV_BF16 = 0
+HS_KV_FP8 = 1
+FP8_ROW_BYTES = 656
+
 DEV_ERR_RANGE = 1
 DEV_ERR_DUPLICATE = 2
 DEV_ERR_CAPACITY = 4
@@ -53,7 +57,7 @@ class hs_pool_desc(ctypes.Structure):
     _fields_ = [("num_requests", ctypes.c_int32), ("num_layers", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("hot_slots", ctypes.c_int32),
                 ("page_tokens", ctypes.c_int32), ("row_elems", ctypes.c_int32),
-                ("max_pages", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("max_pages", ctypes.c_int32), ("kv_format", ctypes.c_int32),
                 ("host_tokens", ctypes.c_int64), ("resident_blocks", ctypes.c_int64)]
 
 

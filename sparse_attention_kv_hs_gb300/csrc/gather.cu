@@ -73,7 +73,7 @@ extern "C" hs_status hs_gather(hs_pool* p, int32_t layer, const int32_t* row_ids
   if (!p || layer < 0 || layer >= p->d.num_layers || n_rows < 0) return HS_ERR_INVALID;
   if (n_rows == 0) return HS_OK;
   if (!row_ids || !out_rows || (reinterpret_cast<uintptr_t>(out_rows) & 15)) return HS_ERR_INVALID;
-  const int rv = p->d.row_elems / 8;
+  const int rv = (int)(hs_row_bytes(p->d) / 16);
   const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
   const uint4* base = static_cast<const uint4*>(p->kv_pool) + (int64_t)layer * rows_in_layer * rv;
   cudaStream_t s = hs_stream(stream);

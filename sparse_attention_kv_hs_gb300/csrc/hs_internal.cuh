@@ -52,6 +52,11 @@ struct hs_pool {
 
 static inline cudaStream_t hs_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Bytes of one KV row in the pool's format (a multiple of 16).
+static inline int64_t hs_row_bytes(const hs_pool_desc& d) {
+  return d.kv_format == HS_KV_FP8 ? 656 : (int64_t)d.row_elems * 2;
+}
+
 // Launch wrappers implemented per translation unit.
 // max_cluster > 0 caps RESOLVE's CTAs per unit (to leave SMs to a kernel that
 // runs beside it); 0 = as many as fit.

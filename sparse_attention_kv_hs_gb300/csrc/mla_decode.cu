@@ -974,7 +974,8 @@ hs_status hs_attn_workspace_init(hs_pool* p) {
   p->attn_ml = nullptr;
   p->attn_max_splits = 0;
   p->attn_kv_maps = nullptr;
-  if (p->d.row_elems != kD) return HS_OK;  // attention needs 576-wide rows; decode call rejects
+  // attention needs 576-wide bf16 rows; the decode calls reject other pools
+  if (p->d.row_elems != kD || p->d.kv_format != HS_KV_BF16) return HS_OK;
   HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)kSmemBytes));
   const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;

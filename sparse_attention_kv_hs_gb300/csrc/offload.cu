@@ -65,7 +65,7 @@ extern "C" hs_status hs_offload_prefix(hs_pool* p, int32_t req, int32_t page, vo
   cudaStream_t ms = hs_stream(main_stream), ss = hs_stream(side_stream);
   HS_CUDA_TRY(cudaEventRecord(p->order_event, ms));
   HS_CUDA_TRY(cudaStreamWaitEvent(ss, p->order_event, 0));
-  const int rv = p->d.row_elems / 8;
+  const int rv = (int)(hs_row_bytes(p->d) / 16);
   const int64_t n = (int64_t)p->d.page_tokens * rv;
   int gx = (int)((n + 255) / 256);
   if (gx > 16) gx = 16;  // 16 CTAs per layer: a page is ~295 KB per layer

@@ -117,7 +117,9 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
   const hs_pool_desc& d = *desc;
   if (d.num_requests <= 0 || d.num_layers <= 0 || d.top_k <= 0 || d.hot_slots <= 0 ||
       d.page_tokens <= 0 || d.row_elems <= 0 || d.row_elems % 8 != 0 || d.max_pages <= 0 ||
-      d.reserved != 0 || d.host_tokens <= 0 || d.resident_blocks < 0 ||
+      (d.kv_format != HS_KV_BF16 && d.kv_format != HS_KV_FP8) ||
+      (d.kv_format == HS_KV_FP8 && d.row_elems != 576) || d.host_tokens <= 0 ||
+      d.resident_blocks < 0 ||
       d.hot_slots % d.page_tokens != 0)
     return HS_ERR_INVALID;
   // Limits of the RESOLVE kernel's shared-memory plan (one CTA per unit).
@@ -155,9 +157,9 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
     delete p;
     return HS_ERR_OOM;
   }
-  p->kv_bytes = (size_t)L * bpl * d.page_tokens * d.row_elems * 2;
+  p->kv_bytes = (size_t)L * bpl * d.page_tokens * hs_row_bytes(d);
   if ((st = dev_alloc(reinterpret_cast<char**>(&p->kv_pool), p->kv_bytes)) != HS_OK) goto fail;
-  p->host_bytes = (size_t)L * d.host_tokens * d.row_elems * 2;
+  p->host_bytes = (size_t)L * d.host_tokens * hs_row_bytes(d);
   {
     cudaError_t e = cudaHostAlloc(&p->host_pool, p->host_bytes,
                                   cudaHostAllocMapped | cudaHostAllocPortable);
@@ -289,14 +291,14 @@ extern "C" hs_status hs_load_page(hs_pool* p, int32_t req, int32_t page, int32_t
     return HS_ERR_INVALID;
   if (block < p->hot_blocks || block >= p->blocks_per_layer) return HS_ERR_INVALID;
   const int64_t off = p->host_off_mirror[req];  // as last set by hs_set_request
-  const int64_t P = p->d.page_tokens, E = p->d.row_elems;
+  const int64_t P = p->d.page_tokens, RB = hs_row_bytes(p->d);
   if (off + (int64_t)(page + 1) * P > p->d.host_tokens) return HS_ERR_INVALID;
-  const size_t bytes = (size_t)P * E * 2;
+  const size_t bytes = (size_t)P * RB;
   for (int32_t l = 0; l < p->d.num_layers; ++l) {
     const char* src = static_cast<const char*>(p->host_pool) +
-                      ((size_t)l * p->d.host_tokens + off + (size_t)page * P) * E * 2;
+                      ((size_t)l * p->d.host_tokens + off + (size_t)page * P) * RB;
     char* dst = static_cast<char*>(p->kv_pool) +
-                (((size_t)l * p->blocks_per_layer + block) * P) * E * 2;
+                (((size_t)l * p->blocks_per_layer + block) * P) * RB;
     HS_CUDA_TRY(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, hs_stream(stream)));
   }
   return hs_map_page(p, req, page, block, stream);

@@ -718,7 +718,7 @@ hs_status launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers, in
   a.B = p->d.hot_slots;
   a.P = p->d.page_tokens;
   a.max_pages = p->d.max_pages;
-  a.row_vec = p->d.row_elems / 8;
+  a.row_vec = (int32_t)(hs_row_bytes(p->d) / 16);
   a.sel_bits = ceil_log2(2 * (int64_t)a.K) < 5 ? 5 : ceil_log2(2 * (int64_t)a.K);
   a.kpt = (a.K + kThreads - 1) / kThreads;
   a.bpt = (a.B + kThreads - 1) / kThreads;

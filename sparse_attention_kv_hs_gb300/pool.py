@@ -31,13 +31,16 @@ class Pool:
 
     def __init__(self, num_requests: int, num_layers: int, top_k: int, hot_slots: int,
                  page_tokens: int, row_elems: int, max_pages: int, host_tokens: int,
-                 resident_blocks: int):
+                 resident_blocks: int, kv_format: int = 0):
         self.R, self.L, self.K, self.B, self.P = (num_requests, num_layers, top_k, hot_slots,
                                                   page_tokens)
         self.row_elems, self.max_pages = row_elems, max_pages
         self.host_tokens, self.resident_blocks = host_tokens, resident_blocks
+        self.kv_format = kv_format
+        # a row's width in 2-byte units: row_elems bf16 values, or 656 FP8-row bytes
+        self.row_units = 656 // 2 if kv_format == 1 else row_elems
         desc = hs_pool_desc(num_requests, num_layers, top_k, hot_slots, page_tokens, row_elems,
-                            max_pages, 0, host_tokens, resident_blocks)
+                            max_pages, kv_format, host_tokens, resident_blocks)
         self.handle = hs_pool_create(desc)
         v = hs_pool_get_views(self.handle)
         self.raw = v
@@ -45,7 +48,7 @@ class Pool:
         self.hot_blocks = num_requests * (hot_slots // page_tokens)
         rows = self.blocks_per_layer * page_tokens
         # device views
-        self.kv_pool = device_tensor(v.kv_pool, (num_layers, rows, row_elems), "<i2")
+        self.kv_pool = device_tensor(v.kv_pool, (num_layers, rows, self.row_units), "<i2")
         self.page_table = device_tensor(v.page_table, (num_requests, max_pages))
         self.ctx_len = device_tensor(v.ctx_len, (num_requests,))
         self.host_off = device_tensor(v.host_off, (num_requests,), "<i8")
@@ -55,10 +58,11 @@ class Pool:
         self.lru_order = device_tensor(v.lru_order, (num_layers, num_requests, hot_slots))
         self.step = device_tensor(v.step, (1,))
         self.error_word = device_tensor(v.error_word, (1,))
-        # host view of the pinned pool (raw bf16 bits)
-        n = num_layers * host_tokens * row_elems
+        # host view of the pinned pool (raw row bits in 2-byte units)
+        n = num_layers * host_tokens * self.row_units
         buf = (ctypes.c_uint16 * n).from_address(v.host_pool)
-        self.host_pool = np.ctypeslib.as_array(buf).reshape(num_layers, host_tokens, row_elems)
+        self.host_pool = np.ctypeslib.as_array(buf).reshape(num_layers, host_tokens,
+                                                             self.row_units)
         self.host_pool_addr = int(v.host_pool)
 
     def hot_row(self, req: int, slot: int) -> int:

@@ -17,7 +17,7 @@ from synth import workloads as W
 HOST_THREADS = max(1, min(32, os.cpu_count() or 1))
 
 
-def make_pool(w: W.Workload, scen: W.Scenario):
+def make_pool(w: W.Workload, scen: W.Scenario, kv_format: int = 0):
     """Create the libhs pool for a workload and bring it to its step-0 state:
     every request's full KV in the pinned host pool, resident pages loaded."""
     import torch
@@ -27,7 +27,7 @@ def make_pool(w: W.Workload, scen: W.Scenario):
     max_pages = int((cap.max() + w.P - 1) // w.P)
     resident_blocks = scen.blocks_per_layer - w.R * w.hot_blocks_per_request()
     pool = hs.Pool(w.R, w.L, w.K, w.B, w.P, W.ROW_ELEMS, max_pages, w.host_tokens(),
-                   max(resident_blocks, 1))
+                   max(resident_blocks, 1), kv_format)
     offs = w.host_offsets()
     hp = pool.host_pool
     # Host rows for positions < ctx at step 0; rows of pages appended later are
@@ -36,7 +36,10 @@ def make_pool(w: W.Workload, scen: W.Scenario):
         for r in range(w.R):
             n = int(w.ctx[r])
             base = hp[l, int(offs[r]):int(offs[r]) + n]
-            synth.rows_into(w.seed, r, l, 0, n, W.ROW_ELEMS, base.ctypes.data, HOST_THREADS)
+            if kv_format == 1:  # FP8 rows (656 bytes each)
+                synth.rows_fp8_into(w.seed, r, l, 0, n, base.ctypes.data, HOST_THREADS)
+            else:
+                synth.rows_into(w.seed, r, l, 0, n, W.ROW_ELEMS, base.ctypes.data, HOST_THREADS)
             extra = int(cap[r]) - n
             if extra > 0:
                 hp[l, int(offs[r]) + n:int(offs[r]) + int(cap[r])] = 0
