@@ -55,6 +55,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="attention",
                     choices=("attention", "resolve", "gather", "mixed", "spec"))
+    ap.add_argument("--kv-format", choices=("bf16", "fp8"), default="bf16",
+                    help="KV row format of the attention / resolve / gather workloads: bf16 "
+                         "[576] (1152 B) or FP8 (656 B: E4M3 latent + 4 scales + bf16 rope)")
     ap.add_argument("--e2e-steps", type=int, default=400)
     ap.add_argument("--kernel-steps", type=int, default=500,
                     help="steps of the sequential per-kernel timing pass")
@@ -171,19 +174,28 @@ def build_inputs(w, steps, threads=16):
     return topk, q
 
 
-def make_pool(hs, w, scen, threads=16):
+def row_bytes(fp8):
+    return synth.FP8_ROW_BYTES if fp8 else W.ROW_BYTES
+
+
+def make_pool(hs, w, scen, threads=16, fp8=False):
     """libhs pool at the workload's step-0 state (host pool filled, tail loaded)."""
     import torch
     cap = w.ctx_capacity()
     max_pages = int((cap.max() + w.P - 1) // w.P)
     resident = max(1, scen.blocks_per_layer - w.R * w.hot_blocks_per_request())
-    pool = hs.Pool(w.R, w.L, w.K, w.B, w.P, W.ROW_ELEMS, max_pages, w.host_tokens(), resident)
+    pool = hs.Pool(w.R, w.L, w.K, w.B, w.P, W.ROW_ELEMS, max_pages, w.host_tokens(), resident,
+                   hs.HS_KV_FP8 if fp8 else hs.HS_KV_BF16)
     offs = w.host_offsets()
     for l in range(w.L):
         for r in range(w.R):
             n = int(w.ctx[r])
             base = pool.host_pool[l, int(offs[r]):int(offs[r]) + n]
-            synth.rows_into(w.seed, w.req_base + r, l, 0, n, W.ROW_ELEMS, base.ctypes.data, threads)
+            if fp8:
+                synth.rows_fp8_into(w.seed, w.req_base + r, l, 0, n, base.ctypes.data, threads)
+            else:
+                synth.rows_into(w.seed, w.req_base + r, l, 0, n, W.ROW_ELEMS, base.ctypes.data,
+                                threads)
     stream = torch.cuda.current_stream()
     for r in range(w.R):
         hs.hs_set_request(pool.handle, r, int(w.ctx[r]), int(offs[r]), stream)
@@ -248,10 +260,10 @@ def kernel_source_hash(name):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def ncu_traffic(kernel_file, workload):
+def ncu_traffic(kernel_file, workload, fp8=False):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload}{'_fp8' if fp8 else ''}.json")
     try:
         with open(path) as f:
             d = json.load(f)
@@ -265,11 +277,12 @@ def ncu_traffic(kernel_file, workload):
 
 # ----------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0):
+def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0, fp8=False):
     """Run the CPU oracle (resolve + gather from host full KV + fp64 attention)
     over the first `units` (request, layer) units of the workload, step after
-    step, for about `seconds` after `skip` untimed warm-up steps.  Returns
-    (rows resolved, elapsed s, steps) of the timed steps."""
+    step, for about `seconds` after `skip` untimed warm-up steps.  With fp8 the
+    host KV is FP8 rows, decoded to their values by the oracle as they are
+    gathered.  Returns (rows resolved, elapsed s, steps) of the timed steps."""
     import oracle
     scen = W.Scenario.build(w)
     o = oracle.ResolveOracle(w.R, w.L, w.K, w.B, w.P, w.ctx_capacity(), scen.blocks_per_layer)
@@ -284,7 +297,8 @@ def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0):
     steps = steps_cap or w.steps
     w2 = W.Workload(**{**w.__dict__, "steps": steps})
     tr = {r: w2.trace(r) for r in reqs}
-    full = {(r, l): synth.rows(w.seed, w.req_base + r, l, 0, int(w.ctx[r]), threads=8)
+    gen = synth.rows_fp8 if fp8 else synth.rows
+    full = {(r, l): gen(w.seed, w.req_base + r, l, 0, int(w.ctx[r]), threads=8)
             for (r, l) in sel}  # the host's full KV of the sampled units (not timed)
     qs = {(r, l): synth.q(w.seed, w.req_base + r, l, 0, w.heads) for (r, l) in sel}
     rows_done, t0, t = 0, time.perf_counter(), 0
@@ -294,6 +308,8 @@ def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0):
         for (r, l) in sel:
             rows, _, _ = o.resolve(l, r, tr[r][t, l], t)
             gathered = full[(r, l)][tr[r][t, l]]          # rows at the selected positions
+            if fp8:
+                gathered = oracle.fp8_rows_to_f64(gathered)
             oracle.sparse_mla_decode(qs[(r, l)], gathered, rows >= 0, W.SCALE)
             rows_done += w.K
         t += 1
@@ -302,13 +318,14 @@ def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0):
     return rows_done, time.perf_counter() - t0, t - min(skip, t)
 
 
-def cpu_baseline(w, seconds):
+def cpu_baseline(w, seconds, fp8=False):
     """The oracle timed in a child process with a fixed thread count."""
     cores = os.cpu_count() or 1
     env = dict(os.environ, OPENBLAS_NUM_THREADS=str(cores), OMP_NUM_THREADS=str(cores),
                MKL_NUM_THREADS=str(cores))
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
-           "--workload", w.name, "--cpu-seconds", str(seconds)]
+           "--workload", w.name, "--cpu-seconds", str(seconds),
+           "--kv-format", "fp8" if fp8 else "bf16"]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
     try:
         d = json.loads(r.stdout.strip().splitlines()[-1])
@@ -338,11 +355,13 @@ def run_ours(args):
     w = W.make(args.workload)
     w.req_base = replica_request_base(rank, w.R)
     attention = args.workload == "attention"
+    fp8 = args.kv_format == "fp8"
+    rb = row_bytes(fp8)
     kern_steps = min(args.kernel_steps, args.steps) if attention else 0
     steps_total = args.warmup + args.steps + kern_steps
     topk_h, q_h = build_inputs(w, steps_total)
     scen = W.Scenario.build(w)
-    pool = make_pool(hs, w, scen)
+    pool = make_pool(hs, w, scen, fp8=fp8)
     R, L, K, H = w.R, w.L, w.K, w.heads
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
@@ -355,8 +374,7 @@ def run_ours(args):
     lse_d = torch.empty((L, R, H), dtype=torch.float32, device=dev)
     cnt_d = torch.zeros((steps_total, L, R), dtype=torch.int32, device=dev)
     copy_stream = torch.cuda.Stream(device=dev) if attention else None
-    gather_d = None if attention else torch.empty((R * K, W.ROW_ELEMS), dtype=torch.int16,
-                                                  device=dev)
+    gather_d = None if attention else torch.empty((R * K, rb // 2), dtype=torch.int16, device=dev)
     ph = pool.handle
     step_ptr = pool.step.data_ptr()
     tk_base, tk_stride_t, tk_stride_l = topk_d.data_ptr(), L * R * K * 4, R * K * 4
@@ -445,36 +463,37 @@ def run_ours(args):
     n_launch_res = max(n_ev, 1) * L
     res_avg_s = res_ms * 1e-3 / n_launch_res
     att_avg_s = att_ms * 1e-3 / n_launch_res
-    miss_bytes_per_launch = misses * W.ROW_BYTES / n_launch_res
+    miss_bytes_per_launch = misses * rb / n_launch_res
     # RESOLVE: the miss rows cross the host link (read) and land in HBM
     resolve_roof = {
         "kernel": "resolve_kernel", "bound": "host_link",
         "achieved": miss_bytes_per_launch / res_avg_s / 1e9, "peak": h2d_peak, "unit": "GB/s",
         "peak_source": "in-run pinned cudaMemcpyAsync H2D, 1 GiB, best of 10",
         "frac": miss_bytes_per_launch / res_avg_s / 1e9 / h2d_peak,
-        "traffic": ncu_traffic("resolve.cu", args.workload),
+        "traffic": ncu_traffic("resolve.cu", args.workload, fp8),
         "avg_launch_us": res_avg_s * 1e6, "miss_rows_per_launch": misses / n_launch_res,
     }
     if attention:
         # rows read once + q read + bf16 out written + row ids, per request
-        att_bytes = R * (K * W.ROW_BYTES + H * W.ROW_ELEMS * 2 + H * W.V_DIM * 2 + K * 4)
+        att_bytes = R * (K * rb + H * W.ROW_ELEMS * 2 + H * W.V_DIM * 2 + K * 4)
         att_flops = R * 2.0 * H * K * (W.ROW_ELEMS + W.V_DIM)
         att_roof = {
             "kernel": "mla_decode_kernel (+ split merge)", "bound": "hbm",
             "achieved": att_bytes / att_avg_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": att_bytes / att_avg_s / 1e9 / peaks["hbm_gbs"],
-            "traffic": ncu_traffic("mla_decode.cu", args.workload),
+            "traffic": ncu_traffic("mla_decode.cu", args.workload, fp8),
             "avg_launch_us": att_avg_s * 1e6,
             "tensor_tflops": att_flops / att_avg_s / 1e12,
             "tensor_frac_of_burst_peak": att_flops / att_avg_s / 1e12 / peaks["bf16_tflops"],
         }
     else:
-        g_bytes = R * K * (2 * W.ROW_BYTES + 4)
+        g_bytes = R * K * (2 * rb + 4)
         att_roof = {
             "kernel": "gather_rows_kernel", "bound": "hbm",
             "achieved": g_bytes / att_avg_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": g_bytes / att_avg_s / 1e9 / peaks["hbm_gbs"],
-            "traffic": ncu_traffic("gather.cu", args.workload), "avg_launch_us": att_avg_s * 1e6,
+            "traffic": ncu_traffic("gather.cu", args.workload, fp8),
+            "avg_launch_us": att_avg_s * 1e6,
         }
     dominant = resolve_roof if res_ms >= att_ms else att_roof
     gpu_launches = args.steps * (2 * L + 1)  # RESOLVE + attention (or gather) per layer, step
@@ -491,9 +510,11 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8-e4m3 rows, fp16 MMA operands" if fp8 else "bf16",
             "data": "synthetic (seeded generator; no dataset)",
             "config": {"workload": workload_name(w), "requests_per_gpu": R, "sparse_layers": L,
+                       "kv_rows": kv_rows_name(fp8),
                        "context": int(w.ctx[0]), "top_k": K, "hot_slots": B_of(w),
                        "heads": H if attention else None, "selection": "70% reuse + 30% uniform"
                        if attention else "70/20/10 drift, layers share 80%",
@@ -515,7 +536,7 @@ def run_ours(args):
             "clocks": clock_info,
         }
         if not args.no_cpu_baseline and not args.profile and world == 1:
-            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, fp8)
         print(json.dumps(line))
     pool.close()
     if dist is not None:
@@ -540,6 +561,11 @@ def decode_step_splits(pool, R, K, L):
 
 def B_of(w):
     return w.B
+
+
+def kv_rows_name(fp8):
+    return ("FP8: 512 E4M3 + 4 fp32 scales + 64 bf16 rope (656 B)" if fp8
+            else "bf16 [576] (1152 B)")
 
 
 def workload_name(w):
@@ -583,12 +609,15 @@ def run_mixed(args):
         def one(r):
             topk[:, :, r, :] = w.trace(r)
         list(ex.map(one, range(R)))
-    pool = make_pool(hs, w, scen)
+    fp8 = args.kv_format == "fp8"
+    rb = row_bytes(fp8)
+    pool = make_pool(hs, w, scen, fp8=fp8)
     # rows of every page appended during the run, generated up front (device)
     app = [(t, r, page, blk) for t in range(steps_total) for (r, page, blk) in scen.appends[t]]
-    app_rows = torch.empty((len(app), L, P, W.ROW_ELEMS), dtype=torch.int16, device=dev)
+    app_rows = torch.empty((len(app), L, P, rb // 2), dtype=torch.int16, device=dev)
+    gen = synth.rows_fp8 if fp8 else synth.rows
     for i, (t, r, page, blk) in enumerate(app):
-        rows = np.stack([synth.rows(w.seed, w.req_base + r, l, page * P, P, threads=8)
+        rows = np.stack([gen(w.seed, w.req_base + r, l, page * P, P, threads=8)
                          for l in range(L)])
         app_rows[i].copy_(torch.from_numpy(rows.view(np.int16)))
     topk_d = torch.from_numpy(topk).to(dev)
@@ -673,15 +702,15 @@ def run_mixed(args):
     off_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(first_app, n_app)]
     misses = int(cnt_d[args.warmup:].sum().item())
     res_avg_s = res_ms * 1e-3 / args.steps
-    miss_bytes = misses * W.ROW_BYTES / args.steps
-    page_bytes = L * P * W.ROW_BYTES
+    miss_bytes = misses * rb / args.steps
+    page_bytes = L * P * rb
     off_avg_s = (sum(off_ms) / max(len(off_ms), 1)) * 1e-3
     resolve_roof = {
         "kernel": "resolve_kernel", "bound": "host_link",
         "achieved": miss_bytes / res_avg_s / 1e9, "peak": h2d_peak, "unit": "GB/s",
         "peak_source": "in-run pinned cudaMemcpyAsync H2D, 1 GiB, best of 10",
         "frac": miss_bytes / res_avg_s / 1e9 / h2d_peak,
-        "traffic": ncu_traffic("resolve.cu", "mixed"), "avg_launch_us": res_avg_s * 1e6,
+        "traffic": ncu_traffic("resolve.cu", "mixed", fp8), "avg_launch_us": res_avg_s * 1e6,
         "miss_rows_per_launch": misses / args.steps,
     }
     off_roof = {
@@ -697,9 +726,9 @@ def run_mixed(args):
             "metric": METRIC, "value": weak_scaling_rate(R * K * L, args.steps, world, elapsed_ms),
             "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16",
+            "vs_baseline": None, "dtype": "fp8-e4m3 rows (moved as bytes)" if fp8 else "bf16",
             "data": "synthetic (seeded generator; no dataset)",
-            "config": {"workload": (f"mixed: {R} requests x {L} sparse layer, ctx log-uniform "
+            "config": {"kv_rows": kv_rows_name(fp8), "workload": (f"mixed: {R} requests x {L} sparse layer, ctx log-uniform "
                                     f"16384..1048576, top-K {K}, B {w.B}, tail 4096; a quarter "
                                     "zero-residency, a quarter fully resident; "
                                     f"{w.appends_per_step} page appends + offloads per step"),
@@ -756,7 +785,9 @@ def run_spec(args):
                 for k in range(T):
                     q[t, l, r, k] = synth.q(w.seed, w.req_base + r, l, t * T + k, H)
     scen = W.Scenario.build(w)
-    pool = make_pool(hs, w, scen)
+    fp8 = args.kv_format == "fp8"
+    rb = row_bytes(fp8)
+    pool = make_pool(hs, w, scen, fp8=fp8)
     topk_d = torch.from_numpy(topk).to(dev)
     q_d = torch.from_numpy(q.view(np.int16)).to(dev)
     rows_d = torch.empty((L, R, T, K), dtype=torch.int32, device=dev)
@@ -810,9 +841,9 @@ def run_spec(args):
     res_s = sum(e[0][l].elapsed_time(e[1][l]) for e in evs for l in range(L)) * 1e-3 / n_launch
     att_s = sum(e[1][l].elapsed_time(e[2][l]) for e in evs for l in range(L)) * 1e-3 / n_launch
     misses = int(cnt_d[args.warmup:].sum().item())
-    miss_bytes = misses * W.ROW_BYTES / n_launch
+    miss_bytes = misses * rb / n_launch
     n_rows = R * T  # decode rows of one attention launch
-    att_bytes = n_rows * (K * W.ROW_BYTES + H * W.ROW_ELEMS * 2 + H * W.V_DIM * 2 + K * 4)
+    att_bytes = n_rows * (K * rb + H * W.ROW_ELEMS * 2 + H * W.V_DIM * 2 + K * 4)
     resolve_roof = {
         "kernel": "resolve_kernel (T = 2 verify tokens)", "bound": "host_link",
         "achieved": miss_bytes / res_s / 1e9, "peak": h2d_peak, "unit": "GB/s",
@@ -831,8 +862,9 @@ def run_spec(args):
             "metric": METRIC, "value": weak_scaling_rate(R * L * T * K, args.steps, world, elapsed_ms),
             "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator; no dataset)",
-            "config": {"workload": (f"spec: {R} requests x {L} sparse layers, ctx {int(w.ctx[0])}, "
+            "vs_baseline": None, "dtype": "fp8-e4m3 rows, fp16 MMA operands" if fp8 else "bf16",
+            "data": "synthetic (seeded generator; no dataset)",
+            "config": {"kv_rows": kv_rows_name(fp8), "workload": (f"spec: {R} requests x {L} sparse layers, ctx {int(w.ctx[0])}, "
                                     f"top-K {K}, {T} verify tokens, B {w.B}, {H} heads"),
                        "l2": "inputs larger than L2, no flush", "parallelism": f"replicas x{world}"},
             "verify_tok_s": weak_scaling_rate(R * T, args.steps, world, elapsed_ms),
@@ -856,6 +888,7 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
     next step (outputs are double-buffered)."""
     R, L, K, H = w.R, w.L, w.K, w.heads
     attention = w.name == "attention"
+    rb = row_bytes(args.kv_format == "fp8")
     steps = min(args.e2e_steps, topk_h.shape[0] - args.warmup)
     hs.hs_pool_reset(pool.handle, stream)
     tk_pin = torch.from_numpy(topk_h).pin_memory()
@@ -869,8 +902,8 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
         res_h = [(torch.empty((L, R, H, W.V_DIM), dtype=torch.bfloat16).pin_memory(),
                   torch.empty((L, R, H), dtype=torch.float32).pin_memory()) for _ in range(2)]
     else:
-        res_d = [(torch.empty((R * K, W.ROW_ELEMS), dtype=torch.int16, device=dev),) for _ in range(2)]
-        res_h = [(torch.empty((R * K, W.ROW_ELEMS), dtype=torch.int16).pin_memory(),)
+        res_d = [(torch.empty((R * K, rb // 2), dtype=torch.int16, device=dev),) for _ in range(2)]
+        res_h = [(torch.empty((R * K, rb // 2), dtype=torch.int16).pin_memory(),)
                  for _ in range(2)]
     sptr = stream.cuda_stream
     copy_stream = torch.cuda.Stream(device=dev) if attention else None
@@ -922,7 +955,7 @@ def run_e2e(torch, hs, lib, pool, w, topk_h, q_h, args, stream, dev, dist, world
     if hs.hs_check_errors(pool.handle):
         raise RuntimeError("device error word set in the e2e run")
     h2d = L * R * K * 4 + (L * R * H * W.ROW_ELEMS * 2 if attention else 0)
-    d2h = (L * R * H * (W.V_DIM * 2 + 4)) if attention else R * K * W.ROW_BYTES
+    d2h = (L * R * H * (W.V_DIM * 2 + 4)) if attention else R * K * rb
     return {"value": weak_scaling_rate(L * R * K, steps, world, ms), "unit": "rows/s",
             "steps": steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "overlap": "read-back of step t on a second stream beside step t+1"}
@@ -943,7 +976,7 @@ def run_reference(args):
     units = 2
     # the warm-up steps run untimed, then `steps` timed steps
     rows, secs, done = oracle_sample(w, seconds=1e9, units=units, steps_cap=total,
-                                     skip=args.warmup)
+                                     skip=args.warmup, fp8=args.kv_format == "fp8")
     per_step = secs / max(done, 1)
     value = units * w.K / per_step
     cores = os.cpu_count() or 1
@@ -952,7 +985,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generator; no dataset)", "impl": "reference",
-        "config": {"workload": workload_name(w), "sample": f"{units} units per step"},
+        "config": {"workload": workload_name(w), "sample": f"{units} units per step",
+                   "kv_rows": kv_rows_name(args.kv_format == "fp8")},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
                          "sample": f"{units} (request, layer) units per step, {done} steps"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
@@ -965,7 +999,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.cpu_baseline_child:
         w = W.make(args.workload)
-        rows, secs, steps = oracle_sample(w, args.cpu_seconds, units=8, steps_cap=512)
+        rows, secs, steps = oracle_sample(w, args.cpu_seconds, units=8, steps_cap=512,
+                                          fp8=args.kv_format == "fp8")
         print(json.dumps({"value": rows / secs, "unit": "rows/s", "kind": "oracle",
                           "sample": f"8 (request, layer) units x {steps} steps "
                                     f"(resolve + gather + fp64 attention), {secs:.1f} s"}))

@@ -41,9 +41,11 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <new>
+#include <string.h>
 
 #include "hs_internal.cuh"
 #include "sm100_ptx.cuh"
@@ -77,6 +79,7 @@ constexpr int kRegsWG0 = 64, kRegsLoad = 168, kRegsMath = 112;
 static_assert(kRegsWG0 + 2 * kRegsLoad + kRegsMath == 4 * 128, "register split");
 static_assert(65536 / 512 == 128, "launch allocation per thread");
 constexpr int kCbK = kD / 64;      // 9 swizzled 128-byte column blocks per K row
+constexpr int kFp8RowBytes = 656;  // an FP8 KV row (HS_KV_FP8)
 
 constexpr uint32_t kBlockBytes = kTile * 128;              // one column block of a tile: 8192
 constexpr uint32_t kStageBytes = kCbK * kBlockBytes;       // 73728
@@ -135,6 +138,9 @@ constexpr uint32_t TM_S = 288;   // CTA 0: S, 3 x 64 columns
 constexpr uint32_t TM_O = 0;     // CTA 1: O, 512 columns
 
 constexpr uint32_t kIdescS = idesc_bf16(128, kTile, false, false);  // A (TMEM), B K-major
+// the same with fp16 A and B (format code 0): FP8 rows
+constexpr uint32_t kIdescS16 = (1u << 4) | ((uint32_t)(kTile >> 3) << 17) |
+                               ((uint32_t)(128 >> 4) << 24);
 // kind::f16 with fp16 A and B (format code 0), fp32 D; A K-major, B MN-major
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((uint32_t)(256 >> 3) << 17) |
                               ((uint32_t)(128 >> 4) << 24);
@@ -142,7 +148,8 @@ constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((uint32_t)(256 >> 3) << 
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before giving up
 
 struct AttnArgs {
-  const uint4* kv;          // this layer's rows, [rows_in_layer][576] bf16 as 16-byte chunks
+  const uint4* kv;          // this layer's rows: [rows_in_layer][576] bf16 as 16-byte chunks,
+                            // or [rows_in_layer][656 bytes] FP8 rows
   const int32_t* row_ids;   // [R][K]
   uint16_t* out;            // [R][H][512] bf16 (splits == 1)
   float* lse;               // [R][H] or null (splits == 1)
@@ -304,8 +311,12 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
 // 16*(lt/64) .. +15 of every tile, so its shared-memory offsets are fixed and
 // its row ids come in 16-byte reads.  Each thread keeps two tiles of loads in
 // flight (the loads for tile t+2 are issued as soon as tile t is stored).
-// TO_F16 converts the values to fp16 on the way.  A row id of -1 stores zeros.
+// The bf16 values are converted to fp16 on the way.  A row id of -1 stores
+// zeros.
 struct ValueLoader {
+  struct Regs {
+    uint4 v[16];
+  };
   const uint4* col;  // chunk c of row 0
   const int32_t* s_rid;
   uint32_t stage0, soff, c7s;
@@ -320,7 +331,7 @@ struct ValueLoader {
     soff = (uint32_t)((c >> 3) * kBlockBytes + r0 * 128);
     c7s = (uint32_t)(c & 7) << 4;
   }
-  __device__ __forceinline__ void issue(int t, uint4 (&v)[16]) const {
+  __device__ __forceinline__ void issue(int t, Regs& R) const {
     const int32_t* rid = s_rid + t * kTile + r0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -328,42 +339,229 @@ struct ValueLoader {
       const int32_t ids[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        v[4 * i + j] = ids[j] >= 0 ? ld_row_chunk(col, ids[j]) : make_uint4(0u, 0u, 0u, 0u);
+        R.v[4 * i + j] = ids[j] >= 0 ? ld_row_chunk(col, ids[j]) : make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  template <bool TO_F16>
-  __device__ __forceinline__ void store(int t, uint4 (&v)[16], uint32_t& vmax) const {
+  __device__ __forceinline__ void store(int t, Regs& R, uint32_t& vmax) const {
     const uint32_t stage = stage0 + (uint32_t)(t % kStages) * kStageBytes;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      uint4 x = v[k];
-      if (TO_F16) {
-        vmax = max_u16x2(vmax, x.x & 0x7fff7fffu);
-        vmax = max_u16x2(vmax, x.y & 0x7fff7fffu);
-        vmax = max_u16x2(vmax, x.z & 0x7fff7fffu);
-        vmax = max_u16x2(vmax, x.w & 0x7fff7fffu);
-        x.x = bf16x2_to_f16x2(x.x);
-        x.y = bf16x2_to_f16x2(x.y);
-        x.z = bf16x2_to_f16x2(x.z);
-        x.w = bf16x2_to_f16x2(x.w);
-      }
+      uint4 x = R.v[k];
+      vmax = max_u16x2(vmax, x.x & 0x7fff7fffu);
+      vmax = max_u16x2(vmax, x.y & 0x7fff7fffu);
+      vmax = max_u16x2(vmax, x.z & 0x7fff7fffu);
+      vmax = max_u16x2(vmax, x.w & 0x7fff7fffu);
+      x.x = bf16x2_to_f16x2(x.x);
+      x.y = bf16x2_to_f16x2(x.y);
+      x.z = bf16x2_to_f16x2(x.z);
+      x.w = bf16x2_to_f16x2(x.w);
       // row r0 + k: r0 % 8 == 0, so its swizzle phase is k % 8
       st_shared_v4(stage + soff + (uint32_t)k * 128u + (c7s ^ ((uint32_t)(k & 7) << 4)), x);
     }
   }
+  // vmax holds bf16 magnitudes: 0x4780 is bf16 65536, from which up (inf and
+  // NaN included) fp16 cannot hold the value
+  __device__ __forceinline__ static bool overflow(uint32_t vmax) {
+    return (vmax & 0xffffu) >= 0x4780u || (vmax >> 16) >= 0x4780u;
+  }
 };
 
-// The loader warps' loop.  The first store waits for q_ready_bar if it is
-// non-zero (Q occupies the stage region until it has moved to TMEM).  Returns
-// error bits.
-template <bool TO_F16>
-__device__ __forceinline__ int load_values(const ValueLoader& L, int n_tiles, uint32_t bar_full0,
-                                           uint32_t bar_empty0, uint32_t q_ready_bar,
-                                           volatile int* abort_flag, int32_t* error_word) {
-  uint32_t vmax = 0;  // per-halfword max of |bf16| bit patterns seen (TO_F16)
+// ---- FP8 rows (656 bytes: 512 E4M3 latent codes, 4 fp32 scales for groups of
+// 128 latent values, 64 bf16 rope values).  Both CTAs turn them into fp16
+// operands on the way into shared memory: latent value = E4M3 * scale, in
+// fp32, rounded once to fp16; rope bf16 -> fp16.
+
+__device__ __forceinline__ uint4 ld_nc_v4(const unsigned char* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+// Four E4M3 codes (one 32-bit word, lowest byte first) times `scale` -> two
+// fp16x2 words.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t w, float scale) {
+  const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+  const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  return make_uint2(pack_f16x2(a.x * scale, a.y * scale), pack_f16x2(b.x * scale, b.y * scale));
+}
+// Two E4M3 codes (low byte first) -> the same two values as fp16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+  uint32_t r;
+  asm("{\n .reg .b16 c;\n cvt.u16.u32 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;\n}" : "=r"(r) : "r"(codes));
+  return r;
+}
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// Lane-wise maximum that returns NaN where either input is NaN.
+__device__ __forceinline__ uint32_t max_nan_f16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ void max_f16(uint32_t& vmax, uint4 x) {
+  vmax = max_u16x2(vmax, x.x & 0x7fff7fffu);
+  vmax = max_u16x2(vmax, x.y & 0x7fff7fffu);
+  vmax = max_u16x2(vmax, x.z & 0x7fff7fffu);
+  vmax = max_u16x2(vmax, x.w & 0x7fff7fffu);
+}
+// vmax holds fp16 magnitudes: 0x7C00 and up is inf or NaN (the value overflowed)
+__device__ __forceinline__ bool f16_overflow(uint32_t vmax) {
+  return (vmax & 0xffffu) >= 0x7C00u || (vmax >> 16) >= 0x7C00u;
+}
+
+// FP8 rows into the stage ring as fp16, for either CTA: ROPE (score CTA) the
+// whole 576 columns, else (value CTA) the 512 latent columns.  Warp lw owns
+// rows 8lw .. 8lw+7 of every tile, lane (rs, k) = (lane / 8, lane % 8) rows
+// 8lw+rs and 8lw+4+rs; for each row it reads latent bytes 128j+16k .. +15
+// (j = 0..3: group j, so one warp instruction covers four rows' 128-byte runs),
+// the row's four scales (16 bytes shared by its 8 lanes) and rope bytes
+// 528+16k .. +15.  16 codes make two 8-column fp16 chunks: columns 128j+16k+8h
+// sit in column block 2j + k/4 at chunk position 2(k%4)+h; rope chunk k in
+// block 8 at position k (positions swizzled with row % 8; the eight lanes of
+// a row, which the shared-memory pipe serves together, hit eight different
+// positions in every store).
+template <bool ROPE>
+struct Fp8Loader {
+  struct Regs {
+    uint4 lat[2][4];
+    uint4 sc[2];
+    uint4 rope[ROPE ? 2 : 1];
+  };
+  const unsigned char* kv;  // the layer's rows, 656 bytes each
+  const int32_t* s_rid;
+  uint32_t stage0;
+  int row0, k;
+
+  __device__ __forceinline__ Fp8Loader(const unsigned char* kv_, const int32_t* s_rid_,
+                                       uint32_t stage0_, int lt)
+      : kv(kv_), s_rid(s_rid_), stage0(stage0_) {
+    const int lane = lt & 31;
+    row0 = (lt >> 5) * 8 + (lane >> 3);
+    k = lane & 7;
+  }
+  __device__ __forceinline__ void issue(int t, Regs& R) const {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int32_t id = s_rid[t * kTile + row0 + 4 * rr];
+      if (id >= 0) {
+        const unsigned char* b = kv + (int64_t)id * kFp8RowBytes;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) R.lat[rr][j] = ld_nc_v4(b + 128 * j + 16 * k);
+        R.sc[rr] = ld_nc_v4(b + 512);
+        if (ROPE) R.rope[rr] = ld_nc_v4(b + 528 + 16 * k);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) R.lat[rr][j] = make_uint4(0u, 0u, 0u, 0u);
+        R.sc[rr] = make_uint4(0u, 0u, 0u, 0u);
+        if (ROPE) R.rope[rr] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+  // A scale for which E4M3 x scale is formed in fp16: 0, or a normal fp16
+  // value small enough that no finite code (|E4M3| <= 448) passes fp16's
+  // largest value (448 x 146 = 65408).  NaN and infinity fail the test.
+  __device__ __forceinline__ static bool fp16_scale(uint32_t bits) {
+    const float s = fabsf(__uint_as_float(bits));
+    return s == 0.f || (s >= 0x1p-14f && s <= 146.f);
+  }
+  // FAST: the products in fp16 (scale rounded to fp16, then one rounding of
+  // the product), with only NaN codes to detect.  Otherwise in fp32 (one
+  // rounding to fp16) with a range check of every value.
+  template <bool FAST>
+  __device__ __forceinline__ void store_rows(int t, Regs& R, uint32_t& vmax) const {
+    const uint32_t stage = stage0 + (uint32_t)(t % kStages) * kStageBytes;
+    uint32_t nan0 = 0, nan1 = 0;  // NaN-propagating maxima (fp16x2)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const int row = row0 + 4 * rr;
+      const uint32_t base = stage + (uint32_t)row * 128u, ph = (uint32_t)(row & 7);
+      const float sc[4] = {__uint_as_float(R.sc[rr].x), __uint_as_float(R.sc[rr].y),
+                           __uint_as_float(R.sc[rr].z), __uint_as_float(R.sc[rr].w)};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 src = R.lat[rr][j];
+        const uint32_t cb = (uint32_t)(2 * j + (k >> 2));
+        uint4 half[2];
+        if (FAST) {
+          const uint32_t s2 = pack_f16x2(sc[j], sc[j]);
+          const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            o[2 * q] = mul_f16x2(e4m3x2_to_f16x2(w[q] & 0xffffu), s2);
+            o[2 * q + 1] = mul_f16x2(e4m3x2_to_f16x2(w[q] >> 16), s2);
+            nan0 = max_nan_f16x2(nan0, o[2 * q]);
+            nan1 = max_nan_f16x2(nan1, o[2 * q + 1]);
+          }
+          half[0] = make_uint4(o[0], o[1], o[2], o[3]);
+          half[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint2 lo = e4m3x4_to_f16x4(h ? src.z : src.x, sc[j]);
+            const uint2 hi = e4m3x4_to_f16x4(h ? src.w : src.y, sc[j]);
+            half[h] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            max_f16(vmax, half[h]);
+          }
+        }
+        // 16-byte stores are served eight lanes at a time: lanes k and k+4
+        // of a row share chunk positions, so they store the two halves in
+        // opposite orders
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int h = i ^ (k >> 2);
+          const uint32_t c = (uint32_t)(2 * (k & 3) + h);
+          st_shared_v4(base + cb * kBlockBytes + ((c ^ ph) << 4), h ? half[1] : half[0]);
+        }
+      }
+      if (ROPE) {
+        uint4 x = R.rope[rr];
+        x.x = bf16x2_to_f16x2(x.x);
+        x.y = bf16x2_to_f16x2(x.y);
+        x.z = bf16x2_to_f16x2(x.z);
+        x.w = bf16x2_to_f16x2(x.w);
+        max_f16(vmax, x);
+        st_shared_v4(base + 8u * kBlockBytes + (((uint32_t)k ^ ph) << 4), x);
+      }
+    }
+    if (FAST) {
+      const uint32_t n = max_nan_f16x2(nan0, nan1);
+      if ((n & 0x7fffu) > 0x7c00u || (n & 0x7fff0000u) > 0x7c000000u) vmax |= 0x7C00u;
+    }
+  }
+  // The fp16 products are taken when every scale of the warp's rows allows
+  // them (one branch per warp and tile).
+  __device__ __forceinline__ void store(int t, Regs& R, uint32_t& vmax) const {
+    bool fast = true;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+      fast = fast && fp16_scale(R.sc[rr].x) && fp16_scale(R.sc[rr].y) &&
+             fp16_scale(R.sc[rr].z) && fp16_scale(R.sc[rr].w);
+    if (__all_sync(0xffffffffu, fast))
+      store_rows<true>(t, R, vmax);
+    else
+      store_rows<false>(t, R, vmax);
+  }
+  __device__ __forceinline__ static bool overflow(uint32_t vmax) { return f16_overflow(vmax); }
+};
+
+// The loader warps' loop, for any of the loaders above.  The first store waits
+// for q_ready_bar if it is non-zero (Q occupies the stage region until it has
+// moved to TMEM).  Returns error bits (VALUE if a value overflowed fp16).
+template <typename Loader>
+__device__ __forceinline__ int load_tiles(const Loader& L, int n_tiles, uint32_t bar_full0,
+                                          uint32_t bar_empty0, uint32_t q_ready_bar,
+                                          volatile int* abort_flag, int32_t* error_word) {
+  uint32_t vmax = 0;  // per-halfword max of the magnitudes seen (see Loader::overflow)
   bool need_q = q_ready_bar != 0;
   const int lane = threadIdx.x & 31;
-  auto put = [&](int t, uint4 (&v)[16]) -> bool {
+  auto put = [&](int t, typename Loader::Regs& v) -> bool {
     if (need_q) {
       if (!wait_bar_warp(q_ready_bar, 0, abort_flag, error_word)) return false;
       need_q = false;
@@ -372,13 +570,13 @@ __device__ __forceinline__ int load_values(const ValueLoader& L, int n_tiles, ui
     if (!wait_bar_warp(bar_empty0 + 8u * s, ((uint32_t)(t / kStages) & 1u) ^ 1u, abort_flag,
                        error_word))
       return false;
-    L.store<TO_F16>(t, v, vmax);
+    L.store(t, v, vmax);
     fence_proxy_async_smem();  // generic-proxy stores -> visible to the MMA
     __syncwarp();
     if (lane == 0) mbar_arrive(bar_full0 + 8u * s);
     return true;
   };
-  uint4 va[16], vb[16];  // two tiles of loads in flight
+  typename Loader::Regs va, vb;  // two tiles of loads in flight
   if (n_tiles > 0) L.issue(0, va);
   for (int t = 0; t < n_tiles; t += 2) {
     if (t + 1 < n_tiles) L.issue(t + 1, vb);
@@ -386,11 +584,14 @@ __device__ __forceinline__ int load_values(const ValueLoader& L, int n_tiles, ui
     if (t + 2 < n_tiles) L.issue(t + 2, va);
     if (t + 1 < n_tiles && !put(t + 1, vb)) break;
   }
-  // 0x4780 is bf16 65536: from there up (inf and NaN included) fp16 cannot hold it
-  if (TO_F16 && ((vmax & 0xffffu) >= 0x4780u || (vmax >> 16) >= 0x4780u)) return HS_DEV_ERR_VALUE;
-  return 0;
+  return Loader::overflow(vmax) ? HS_DEV_ERR_VALUE : 0;
 }
 
+// FP8: the pool holds 656-byte FP8 rows (see Fp8Loader); both CTAs load
+// them with vector loads and the MMAs run on fp16 operands (Q converted from
+// bf16 as it moves to tensor memory).  Otherwise the rows are bf16 [576]; CTA
+// 0 gathers them by TMA and the score MMA runs on bf16.
+template <bool FP8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map,
                       const __grid_constant__ CUtensorMap q_map, const AttnArgs a) {
@@ -416,8 +617,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // ---- set-up: barriers, tensor memory ---------------------------------
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
-      // CTA 0: one arm (+ TMA bytes); CTA 1: one arrival per loader warp
-      mbar_init(bar(B_KV_FULL + i), rank == 0 ? 1 : kLoadWarps);
+      // TMA (CTA 0, bf16 rows): one arm (+ the bytes); else one arrival per loader warp
+      mbar_init(bar(B_KV_FULL + i), (rank == 0 && !FP8) ? 1 : kLoadWarps);
       mbar_init(bar(B_KV_EMPTY + i), 1);
     }
     for (int i = 0; i < kSBufs; ++i) {
@@ -497,7 +698,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_RID));
     }
-    if (rank == 0) {
+    if (FP8) {
+      // FP8 rows, both CTAs by vector loads: CTA 0 the whole rows (after Q has
+      // left the stage region), CTA 1 the 512 value columns
+      const unsigned char* kv8 = reinterpret_cast<const unsigned char*>(a.kv);
+      if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word)) {
+        if (rank == 0) {
+          const Fp8Loader<true> L(kv8, s_rid, sbase + OFF_STAGE, lt);
+          err |= load_tiles(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), bar(B_Q_READY),
+                            abort_flag, a.error_word);
+        } else {
+          const Fp8Loader<false> L(kv8, s_rid, sbase + OFF_STAGE, lt);
+          err |= load_tiles(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
+                            a.error_word);
+        }
+      }
+    } else if (rank == 0) {
       // CTA 0: the whole 576-column rows by TMA (written straight into the
       // swizzled stage, one shared-memory pass).  Lanes 0..15 of the eight
       // warps issue the 9 x 16 gathers of 4 rows; a row id of -1 reads past the
@@ -529,8 +745,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word)) {
       // CTA 1: the 512 value columns by vector loads, converted to fp16
       const ValueLoader L(a.kv, s_rid, sbase + OFF_STAGE, lt);
-      err |= load_values<true>(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
-                               a.error_word);
+      err |= load_tiles(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
+                        a.error_word);
     }
     finish();
     return;
@@ -566,7 +782,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kD / 16; ++kk)
             mma_ts_elect(dS, tm + TM_Q + kk * 8,
                          kd + (uint64_t)((((kk >> 2) * kBlockBytes) + (kk & 3) * 32) >> 4),
-                         kIdescS, kk > 0);
+                         FP8 ? kIdescS16 : kIdescS, kk > 0);
           mma_commit_elect(bar(B_KV_EMPTY + s));
           mma_commit_elect(bar(B_S_FULL + b));
         }
@@ -628,10 +844,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int h = tid - kMathWarp0 * 32;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = wait_bar_warp(bar(B_Q_SMEM), 0, abort_flag, a.error_word);
-    if (ok) {  // Q[h] -> TMEM columns TM_Q .. TM_Q+287 (bf16 pairs), zero for padded heads
+    if (ok) {  // Q[h] -> TMEM columns TM_Q .. TM_Q+287 (pairs), zero for padded heads
       // swizzled rows: column block cb holds [128 rows][128 B]; 16-byte chunk c
       // of row h sits at chunk position c ^ (h % 8) (conflict-free reads)
       const unsigned char* qrow = smem + OFF_STAGE + h * 128;
+      uint32_t qmax = 0;  // bf16 magnitudes seen (FP8 rows: Q must fit fp16)
       for (int c0 = 0; c0 < kD / 2; c0 += 16) {
         uint32_t v[16];
         const unsigned char* blk = qrow + (c0 / 32) * kQBlockBytes;
@@ -640,6 +857,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int c = (c0 % 32) / 4 + i;
           uint4 x = make_uint4(0, 0, 0, 0);
           if (h < a.H) x = *reinterpret_cast<const uint4*>(blk + ((c ^ (h & 7)) * 16));
+          if (FP8) {  // the score MMA's operands are fp16
+            qmax = max_u16x2(qmax, x.x & 0x7fff7fffu);
+            qmax = max_u16x2(qmax, x.y & 0x7fff7fffu);
+            qmax = max_u16x2(qmax, x.z & 0x7fff7fffu);
+            qmax = max_u16x2(qmax, x.w & 0x7fff7fffu);
+            x.x = bf16x2_to_f16x2(x.x);
+            x.y = bf16x2_to_f16x2(x.y);
+            x.z = bf16x2_to_f16x2(x.z);
+            x.w = bf16x2_to_f16x2(x.w);
+          }
           v[4 * i + 0] = x.x;
           v[4 * i + 1] = x.y;
           v[4 * i + 2] = x.z;
@@ -648,6 +875,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_st16(tm + lane_off + TM_Q + c0, v);
       }
       tmem_st_wait();
+      if (FP8 && ValueLoader::overflow(qmax)) err |= HS_DEV_ERR_VALUE;
     }
     tc_fence_before();
     mbar_arrive(bar(B_Q_READY));
@@ -950,14 +1178,18 @@ hs_status encode_rows_map(CUtensorMap* m, const void* base, uint64_t rows, uint3
   return cr == CUDA_SUCCESS ? HS_OK : HS_ERR_INVALID;
 }
 
-// Launch the decode kernel (+ the merge when splits > 1).  Arguments checked by the caller.
+// Launch the decode kernel (+ the merge when splits > 1).  Arguments checked by
+// the caller; kv_map is not read for FP8 rows.
 hs_status launch_decode(AttnArgs& a, const CUtensorMap& kv_map, const void* q, int R,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool fp8 = false) {
   CUtensorMap q_map;  // host-side encode only: safe inside stream capture
   if (encode_rows_map(&q_map, q, (uint64_t)R * a.H, kHeads) != HS_OK) return HS_ERR_INVALID;
   const int tiles = (a.K + kTile - 1) / kTile;
   a.rows_per_split = ((tiles + a.splits - 1) / a.splits) * kTile;
-  mla_decode_kernel<<<dim3(2 * a.splits, R), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
+  if (fp8)
+    mla_decode_kernel<true><<<dim3(2 * a.splits, R), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
+  else
+    mla_decode_kernel<false><<<dim3(2 * a.splits, R), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
   HS_CUDA_TRY(cudaGetLastError());
   if (a.splits > 1) {
     merge_splits_kernel<<<dim3(a.H, R), 128, 0, s>>>(a.ws_o, a.ws_lse, a.splits, a.H, a.out,
@@ -967,6 +1199,12 @@ hs_status launch_decode(AttnArgs& a, const CUtensorMap& kv_map, const void* q, i
   return HS_OK;
 }
 
+// First row of `layer` in the device pool (rows of hs_row_bytes each).
+const uint4* layer_rows(const hs_pool* p, int32_t layer, int64_t rows_in_layer) {
+  return reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(p->kv_pool) +
+                                        (int64_t)layer * rows_in_layer * hs_row_bytes(p->d));
+}
+
 }  // namespace
 
 hs_status hs_attn_workspace_init(hs_pool* p) {
@@ -974,15 +1212,22 @@ hs_status hs_attn_workspace_init(hs_pool* p) {
   p->attn_ml = nullptr;
   p->attn_max_splits = 0;
   p->attn_kv_maps = nullptr;
-  // attention needs 576-wide bf16 rows; the decode calls reject other pools
-  if (p->d.row_elems != kD || p->d.kv_format != HS_KV_BF16) return HS_OK;
-  HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kSmemBytes));
+  // attention needs 576-wide rows (bf16, or FP8 whose pool validation fixes
+  // 576); the decode calls reject other pools
+  if (p->d.row_elems != kD) return HS_OK;
+  const bool fp8 = p->d.kv_format == HS_KV_FP8;
+  if (fp8)
+    HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel<true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
+  else
+    HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel<false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
   const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
   CUtensorMap* maps = new (std::nothrow) CUtensorMap[p->d.num_layers];
   if (!maps) return HS_ERR_OOM;
   p->attn_kv_maps = maps;
-  for (int l = 0; l < p->d.num_layers; ++l) {
+  if (fp8) memset(maps, 0, sizeof(CUtensorMap) * p->d.num_layers);  // FP8 rows need no maps
+  for (int l = 0; !fp8 && l < p->d.num_layers; ++l) {
     const void* base = static_cast<const uint16_t*>(p->kv_pool) + (int64_t)l * rows_in_layer * kD;
     const hs_status st = encode_rows_map(&maps[l], base, (uint64_t)rows_in_layer, 1);
     if (st != HS_OK) return st;
@@ -1022,8 +1267,7 @@ hs_status hs_launch_attention(hs_pool* p, int32_t layer, const void* q, const in
   const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
   if (rows_in_layer > INT32_MAX) return HS_ERR_INVALID;
   AttnArgs a;
-  a.kv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p->kv_pool) +
-                                        (int64_t)layer * rows_in_layer * kD);
+  a.kv = layer_rows(p, layer, rows_in_layer);
   a.row_ids = row_ids;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
@@ -1041,7 +1285,7 @@ hs_status hs_launch_attention(hs_pool* p, int32_t layer, const void* q, const in
   }
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_decode(a, static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q,
-                       p->d.num_requests, stream);
+                       p->d.num_requests, stream, p->d.kv_format == HS_KV_FP8);
 }
 
 extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void* q,
@@ -1077,8 +1321,7 @@ extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int3
   if (splits > 1 && n * splits > (int64_t)p->d.num_requests * p->attn_max_splits)
     return HS_ERR_INVALID;  // K too long for this many rows in the workspace
   AttnArgs a;
-  a.kv = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p->kv_pool) +
-                                        (int64_t)layer * rows_in_layer * kD);
+  a.kv = layer_rows(p, layer, rows_in_layer);
   a.row_ids = row_ids;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
@@ -1091,7 +1334,7 @@ extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int3
   a.splits = splits;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_decode(a, static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q, (int)n,
-                       hs_stream(stream));
+                       hs_stream(stream), p->d.kv_format == HS_KV_FP8);
 }
 
 // ---------------------------------------------------------------------------
@@ -1133,8 +1376,8 @@ hs_status noalloc_setup(int dev) {
   void* errw = nullptr;
   HS_CUDA_TRY(cudaGetSymbolAddress(&scratch, g_noalloc_scratch));
   HS_CUDA_TRY(cudaGetSymbolAddress(&errw, g_noalloc_error_word));
-  HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kSmemBytes));
+  HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel<false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
   int sms = 0;
   HS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   g_noalloc_sms[dev] = sms;

@@ -52,6 +52,15 @@ def make_pool(w: W.Workload, scen: W.Scenario, kv_format: int = 0):
     return pool
 
 
+def rows_for_oracle(w: W.Workload, r: int, l: int, pos, kv_format: int = 0) -> np.ndarray:
+    """The KV rows at token positions `pos` of (request r, layer l) as the
+    oracle's attention takes them: bf16 bits, or for FP8 pools the values the
+    656-byte rows stand for (fp64)."""
+    if kv_format == 1:
+        return oracle.fp8_rows_to_f64(synth.rows_fp8_at(w.seed, r, l, pos))
+    return synth.rows_at(w.seed, r, l, pos)
+
+
 def make_oracle(w: W.Workload, scen: W.Scenario) -> oracle.ResolveOracle:
     o = oracle.ResolveOracle(w.R, w.L, w.K, w.B, w.P, w.ctx_capacity(), scen.blocks_per_layer)
     for r in range(w.R):

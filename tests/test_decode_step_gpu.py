@@ -34,9 +34,9 @@ def _queries(w, t):
                      for l in range(w.L)])  # [L][R][H][576] bf16 bits
 
 
-def replay_steps(w, check_steps, same_stream=False, graph=False):
+def replay_steps(w, check_steps, same_stream=False, graph=False, kv_format=0):
     scen = W.Scenario.build(w)
-    pool = harness.make_pool(w, scen)
+    pool = harness.make_pool(w, scen, kv_format)
     o = harness.make_oracle(w, scen)
     tr = harness.traces(w)  # [steps][L][R][K]
     R, K, L, H = w.R, w.K, w.L, w.heads
@@ -83,8 +83,8 @@ def replay_steps(w, check_steps, same_stream=False, graph=False):
                 np.testing.assert_array_equal(rows[l, r], ref_rows, err_msg=f"t={t} l={l} r={r}")
                 assert cnt[l, r] == len(ref_log), (t, l, r)
                 if t in check_steps:
-                    ref, ref_lse = oracle.sparse_mla_decode(
-                        q[l, r], synth.rows_at(w.seed, r, l, tr[t, l, r]), None, W.SCALE)
+                    kv = harness.rows_for_oracle(w, r, l, tr[t, l, r], kv_format)
+                    ref, ref_lse = oracle.sparse_mla_decode(q[l, r], kv, None, W.SCALE)
                     _check(out[l, r], ref, (t, l, r))
                     assert np.allclose(lse[l, r], ref_lse, rtol=0, atol=2e-3)
     assert hs.hs_check_errors(pool.handle) == 0
@@ -113,6 +113,12 @@ def test_decode_step_graph_captured():
     """One step (both streams, events, step counter) captured once, replayed."""
     w = W.make("attention", R=2, L=2, steps=5)
     replay_steps(w, check_steps={0, 2, 4}, graph=True)
+
+
+def test_decode_step_fp8_rows():
+    """The full-size step on a pool of 656-byte FP8 rows."""
+    w = W.make("attention", steps=4)
+    replay_steps(w, check_steps={0, 3}, kv_format=1)
 
 
 def test_decode_step_rejects_bad_arguments():

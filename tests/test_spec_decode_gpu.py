@@ -28,9 +28,9 @@ def _check(got, ref, what=""):
     assert max_abs <= MAX_ABS and mean_rel <= MEAN_REL, (what, max_abs, mean_rel)
 
 
-def replay_tokens(w, attn_steps=(), attn_requests=None):
+def replay_tokens(w, attn_steps=(), attn_requests=None, kv_format=0):
     scen = W.Scenario.build(w)
-    pool = harness.make_pool(w, scen)
+    pool = harness.make_pool(w, scen, kv_format)
     o = harness.make_oracle(w, scen)
     R, L, K, T, H = w.R, w.L, w.K, w.tokens, w.heads
     tr = np.stack([w.trace_tokens(r) for r in range(R)], axis=2)  # [steps][L][R][T][K]
@@ -65,7 +65,7 @@ def replay_tokens(w, attn_steps=(), attn_requests=None):
                 lse = d_lse.cpu().numpy()
                 for r in reqs:
                     for k in range(T):
-                        kv = synth.rows_at(w.seed, r, l, tr[t, l, r, k])
+                        kv = harness.rows_for_oracle(w, r, l, tr[t, l, r, k], kv_format)
                         ref, ref_lse = oracle.sparse_mla_decode(q[r, k], kv, None, W.SCALE)
                         _check(out[r, k], ref, (t, l, r, k))
                         assert np.allclose(lse[r, k], ref_lse, rtol=0, atol=2e-3)
@@ -90,6 +90,12 @@ def test_spec_workload_full_size():
     attention checked on the last step for 4 requests (both tokens)."""
     w = W.make("spec", steps=12)
     replay_tokens(w, attn_steps={11}, attn_requests=[0, 5, 13, 31])
+
+
+def test_spec_workload_fp8_rows():
+    """The scaled-down spec workload on a pool of 656-byte FP8 rows."""
+    w = W.make("spec", R=4, steps=4)
+    replay_tokens(w, attn_steps={0, 3}, kv_format=1)
 
 
 def test_one_token_is_the_plain_resolve():
