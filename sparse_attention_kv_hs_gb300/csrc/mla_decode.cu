@@ -371,6 +371,9 @@ struct ValueLoader {
 // operands on the way into shared memory: latent value = E4M3 * scale, in
 // fp32, rounded once to fp16; rope bf16 -> fp16.
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ uint4 ld_nc_v4(const unsigned char* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -436,16 +439,28 @@ struct Fp8Loader {
   const unsigned char* kv;  // the layer's rows, 656 bytes each
   const int32_t* s_rid;
   uint32_t stage0;
-  int row0, k;
+  int row0, k, lt, n_tiles;
 
   __device__ __forceinline__ Fp8Loader(const unsigned char* kv_, const int32_t* s_rid_,
-                                       uint32_t stage0_, int lt)
-      : kv(kv_), s_rid(s_rid_), stage0(stage0_) {
+                                       uint32_t stage0_, int lt_, int n_tiles_)
+      : kv(kv_), s_rid(s_rid_), stage0(stage0_), lt(lt_), n_tiles(n_tiles_) {
     const int lane = lt & 31;
     row0 = (lt >> 5) * 8 + (lane >> 3);
     k = lane & 7;
   }
+  // Loads tile t into registers, and asks L2 for the rows of tile t+2 (the
+  // next loads of this register set): loader thread lt, the 128-byte lines
+  // 128 (lt % 4) and 128 (lt % 4) + 512 (the latter for lt % 4 < 2) of row
+  // lt / 4, six lines per row.
   __device__ __forceinline__ void issue(int t, Regs& R) const {
+    if (t + 2 < n_tiles) {
+      const int32_t pid = s_rid[(t + 2) * kTile + (lt >> 2)];
+      if (pid >= 0) {
+        const unsigned char* pb = kv + (int64_t)pid * kFp8RowBytes + 128 * (lt & 3);
+        prefetch_l2(pb);
+        if ((lt & 3) < 2) prefetch_l2(pb + 512);
+      }
+    }
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const int32_t id = s_rid[t * kTile + row0 + 4 * rr];
@@ -704,11 +719,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const unsigned char* kv8 = reinterpret_cast<const unsigned char*>(a.kv);
       if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word)) {
         if (rank == 0) {
-          const Fp8Loader<true> L(kv8, s_rid, sbase + OFF_STAGE, lt);
+          const Fp8Loader<true> L(kv8, s_rid, sbase + OFF_STAGE, lt, n_tiles);
           err |= load_tiles(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), bar(B_Q_READY),
                             abort_flag, a.error_word);
         } else {
-          const Fp8Loader<false> L(kv8, s_rid, sbase + OFF_STAGE, lt);
+          const Fp8Loader<false> L(kv8, s_rid, sbase + OFF_STAGE, lt, n_tiles);
           err |= load_tiles(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
                             a.error_word);
         }

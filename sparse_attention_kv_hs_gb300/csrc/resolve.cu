@@ -271,7 +271,8 @@ __device__ __forceinline__ void unstage_rows(const unsigned char* stage, uint4* 
 }
 
 // P_CT / RV_CT: compile-time page size and row width (16-byte vectors) for the
-// common shape (256, 72 = 576 bf16); 0 = take them from the arguments.
+// common shapes (256, 72 = 576 bf16; 256, 41 = a 656-byte FP8 row); 0 = take
+// them from the arguments (the row split c / rv then costs a division).
 //
 // A unit is served by a cluster of C CTAs.  CTA 0 ("metadata") runs steps 1-4
 // for the whole selection.  With C > 1 the other C - 1 CTAs ("fetch") split
@@ -653,6 +654,8 @@ hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes, int max_
   *smem_bytes = smem;
   HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<256, 72>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<256, 41>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   HS_CUDA_TRY(cudaFuncSetAttribute(resolve_kernel<0, 0>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   // How many clusters of 1, 2, 4 and 8 CTAs can run at once: a launch whose
@@ -753,8 +756,10 @@ hs_status launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers, in
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = C > 1 ? 1 : 0;
-  if (a.P == 256 && a.row_vec == 72)
+  if (a.P == 256 && a.row_vec == 72)  // bf16 [576] rows
     HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<256, 72>, a));
+  else if (a.P == 256 && a.row_vec == 41)  // FP8 rows (656 bytes)
+    HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<256, 41>, a));
   else
     HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<0, 0>, a));
   return HS_OK;
