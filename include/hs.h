@@ -71,7 +71,9 @@ typedef enum {
 #define HS_DEV_ERR_INTERNAL 32 /* a kernel found its own launch set-up unusable and did nothing */
 #define HS_DEV_ERR_VALUE 64    /* attention: a value element (first 512 columns of a selected
                                   row) is not finite or has magnitude >= 65536; the P.V
-                                  product runs in fp16 (see hs_sparse_mla_decode) */
+                                  product runs in fp16 (see hs_sparse_mla_decode).  FP8
+                                  rows: an operand (a latent value, a rope value or q)
+                                  that fp16 cannot hold, or a NaN code */
 
 /* KV row formats.  HS_KV_BF16: row_elems bf16 values (2 * row_elems bytes).
  * HS_KV_FP8 (row_elems must be 576): 656 bytes -- bytes 0..511 the 512 latent
@@ -80,7 +82,7 @@ typedef enum {
  * bytes 528..655 the 64 rope values as bf16.  The pages' benchmark runs an FP8
  * KV cache but gives no row layout; this is the one this library defines.
  * RESOLVE, gather, page loads and offload move rows as opaque bytes in
- * either format. */
+ * either format; attention dequantizes FP8 rows (see hs_sparse_mla_decode). */
 enum { HS_KV_BF16 = 0, HS_KV_FP8 = 1 };
 
 typedef struct {
@@ -226,6 +228,12 @@ hs_status hs_gather(hs_pool* pool, int32_t layer, const int32_t* row_ids,
  * 2^-25 each) and gives the probabilities 11 significant bits; a value
  * element that is not finite or has magnitude >= 65536 sets error bit VALUE
  * (that request's output is then not meaningful).
+ * FP8 pools (HS_KV_FP8): both products run on fp16 operands.  q is rounded
+ * from bf16 to fp16; a latent value is E4M3(code) * scale formed as fp16 --
+ * from the scale rounded to fp16 when the row group's scale is 0 or in
+ * [2^-14, 146] (so no code can overflow), else in fp32 and rounded once --
+ * and a rope value is converted from bf16.  An operand fp16 cannot hold, or
+ * a NaN code, sets VALUE.
  *   q        device bf16 [R][num_heads][row_elems]   (num_heads <= 128)
  *   row_ids  device int32 [R][K] (e.g. hs_resolve's output for this layer)
  *   out      device bf16 [R][num_heads][v_dim]
