@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import ctypes
 import hashlib
 import json
 import math
@@ -627,10 +628,10 @@ def run_mixed(args):
     ctx = w.ctx.astype(np.int64).copy()
     ph = pool.handle
     step_ptr = pool.step.data_ptr()
-    n_app = len(app)
-    ev_go = [torch.cuda.Event() for _ in range(n_app)]
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(n_app)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(n_app)]
+    # one offload launch per step (all of the step's completed pages)
+    ev_go = [torch.cuda.Event() for _ in range(steps_total)]
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(steps_total)]
     for e in ev_b:  # torch creates events lazily; the library is handed raw handles
         e.record(side)
     torch.cuda.synchronize()
@@ -657,19 +658,24 @@ def run_mixed(args):
             ev_res[1].record(stream)
         lib.hs_step_advance(step_ptr, sptr)
         launches[0] += 2
-        for (r, page, blk) in scen.appends[t]:
+        apps = scen.appends[t]
+        for (r, page, blk) in apps:
             i = app_index[(t, r, page)]
             pool.kv_pool[0:L, blk * P:(blk + 1) * P].copy_(app_rows[i])  # model writes the page
             call(lib.hs_map_page(ph, r, page, blk, sptr), "map_page")
-            ev_go[i].record(stream)
-            side.wait_event(ev_go[i])
-            ev_a[i].record(side)
-            call(lib.hs_offload_prefix(ph, r, page, sptr, side.cuda_stream, ev_b[i].cuda_event),
-                 "offload")
-            pending[(r, page)] = i
+            pending[(r, page)] = t
             ctx[r] += P
             call(lib.hs_set_request(ph, r, int(ctx[r]), int(offs[r]), sptr), "set_request")
-            launches[0] += 3  # map, offload, set_request (the page copy is a memcpy)
+            launches[0] += 2  # map, set_request (the page copy is a memcpy)
+        if apps:  # the step's completed pages -> host, one launch on the side stream
+            ev_go[t].record(stream)
+            side.wait_event(ev_go[t])
+            ev_a[t].record(side)
+            reqs = (ctypes.c_int32 * len(apps))(*[a[0] for a in apps])
+            pages = (ctypes.c_int32 * len(apps))(*[a[1] for a in apps])
+            call(lib.hs_offload_pages(ph, len(apps), ctypes.addressof(reqs), ctypes.addressof(pages),
+                                      sptr, side.cuda_stream, ev_b[t].cuda_event), "offload")
+            launches[0] += 1
 
     app_index = {(t, r, page): i for i, (t, r, page, blk) in enumerate(app)}
     h2d_peak = measure_h2d_peak(torch) if not args.profile else float("nan")
@@ -685,7 +691,7 @@ def run_mixed(args):
         time.sleep(0.3)
     evr = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     launches[0] = 0
-    first_app = sum(len(scen.appends[t]) for t in range(args.warmup))
+    off_steps = [t for t in range(args.warmup, steps_total) if scen.appends[t]]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t_start.record(stream)
@@ -699,11 +705,12 @@ def run_mixed(args):
     if hs.hs_check_errors(ph):
         raise RuntimeError("device error word set in the mixed run")
     res_ms = sum(e[0].elapsed_time(e[1]) for e in evr)
-    off_ms = [ev_a[i].elapsed_time(ev_b[i]) for i in range(first_app, n_app)]
+    off_ms = [ev_a[t].elapsed_time(ev_b[t]) for t in off_steps]
     misses = int(cnt_d[args.warmup:].sum().item())
     res_avg_s = res_ms * 1e-3 / args.steps
     miss_bytes = misses * rb / args.steps
     page_bytes = L * P * rb
+    off_bytes = page_bytes * sum(len(scen.appends[t]) for t in off_steps) / max(len(off_steps), 1)
     off_avg_s = (sum(off_ms) / max(len(off_ms), 1)) * 1e-3
     resolve_roof = {
         "kernel": "resolve_kernel", "bound": "host_link",
@@ -714,12 +721,12 @@ def run_mixed(args):
         "miss_rows_per_launch": misses / args.steps,
     }
     off_roof = {
-        "kernel": "offload_page_kernel", "bound": "host_link",
-        "achieved": page_bytes / off_avg_s / 1e9 if off_ms else None, "peak": d2h_peak,
+        "kernel": "offload_pages_kernel", "bound": "host_link",
+        "achieved": off_bytes / off_avg_s / 1e9 if off_ms else None, "peak": d2h_peak,
         "unit": "GB/s", "peak_source": "in-run pinned cudaMemcpyAsync D2H, 1 GiB, best of 10",
-        "frac": page_bytes / off_avg_s / 1e9 / d2h_peak if off_ms else None,
+        "frac": off_bytes / off_avg_s / 1e9 / d2h_peak if off_ms else None,
         "traffic": None, "avg_launch_us": off_avg_s * 1e6, "launches": len(off_ms),
-        "bytes_per_launch": page_bytes,
+        "bytes_per_launch": off_bytes, "pages_per_launch": off_bytes / page_bytes,
     }
     if rank == 0:
         line = {

@@ -334,6 +334,20 @@ hs_status hs_offload_prefix(hs_pool* pool, int32_t req, int32_t page,
                             void* main_stream, void* side_stream,
                             void* done_event);
 
+/* Prefix offload of several pages in one launch (e.g. every page a decode
+ * step completed): as hs_offload_prefix for each (reqs[i], pages[i]),
+ * i < num_pages, with one `done_event` recorded after all of them.  Page
+ * "GLM 5.3 Optimizations, Part 1", section "How it works": the completed
+ * prefix is copied to host memory by one launch for all sparse-MLA layers.
+ * reqs and pages are host arrays; 1 <= num_pages <= HS_OFFLOAD_MAX_PAGES.
+ * HS_ERR_INVALID for out-of-range arguments (nothing is launched); a pair
+ * whose page is not mapped to a resident block when the copy runs is skipped
+ * and sets device error bit BLOCK.  The same pair twice copies it twice. */
+#define HS_OFFLOAD_MAX_PAGES 256
+hs_status hs_offload_pages(hs_pool* pool, int32_t num_pages, const int32_t* reqs,
+                           const int32_t* pages, void* main_stream, void* side_stream,
+                           void* done_event);
+
 /* Make `main_stream` wait for `done_event`, then mark the page host only
  * (page_table = -1).  The freed block may be mapped again afterwards. */
 hs_status hs_commit_offload(hs_pool* pool, int32_t req, int32_t page,

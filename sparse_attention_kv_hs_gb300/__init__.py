@@ -33,6 +33,7 @@ DEV_ERR_RANGE = 1
 DEV_ERR_DUPLICATE = 2
 DEV_ERR_CAPACITY = 4
 DEV_ERR_BLOCK = 8
+HS_OFFLOAD_MAX_PAGES = 256  # pages one hs_offload_pages call takes
 DEV_ERR_WAIT = 16
 DEV_ERR_INTERNAL = 32
 DEV_ERR_VALUE = 64
@@ -40,7 +41,7 @@ DEV_ERR_VALUE = 64
 EXPORTED = (
     "hs_pool_create", "hs_pool_destroy", "hs_pool_get_views", "hs_pool_reset",
     "hs_set_request", "hs_map_page", "hs_load_page", "hs_resolve", "hs_gather",
-    "hs_sparse_mla_decode", "hs_offload_prefix", "hs_commit_offload",
+    "hs_sparse_mla_decode", "hs_offload_prefix", "hs_offload_pages", "hs_commit_offload",
     "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
     "hs_sparse_mla_decode_noalloc", "hs_decode_step", "hs_resolve_tokens",
     "hs_sparse_mla_decode_tokens",
@@ -102,6 +103,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_gather": [p, i32, p, i64, p, p],
         "hs_sparse_mla_decode": [p, i32, p, p, i32, i32, f32, p, p, p],
         "hs_offload_prefix": [p, i32, i32, p, p, p],
+        "hs_offload_pages": [p, i32, p, p, p, p, p],
         "hs_commit_offload": [p, i32, i32, p, p],
         "hs_step_advance": [p, p],
         "hs_check_errors": [p, ctypes.POINTER(i32)],
@@ -265,6 +267,18 @@ def hs_decode_step(pool: int, layer_begin: int, num_layers: int, topk_idx, q, nu
 def hs_offload_prefix(pool: int, req: int, page: int, main_stream, side_stream, done_event) -> None:
     _check(load().hs_offload_prefix(pool, req, page, _stream(main_stream), _stream(side_stream),
                                     _event(done_event)), "hs_offload_prefix")
+
+
+def hs_offload_pages(pool: int, reqs, pages, main_stream, side_stream, done_event) -> None:
+    """One launch copying every (reqs[i], pages[i]) page; host sequences."""
+    n = len(reqs)
+    if len(pages) != n:
+        raise HsError(HS_ERR_INVALID, "hs_offload_pages: reqs and pages differ in length")
+    r = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in reqs])
+    g = (ctypes.c_int32 * max(n, 1))(*[int(x) for x in pages])
+    _check(load().hs_offload_pages(pool, n, ctypes.addressof(r), ctypes.addressof(g),
+                                   _stream(main_stream), _stream(side_stream), _event(done_event)),
+           "hs_offload_pages")
 
 
 def hs_commit_offload(pool: int, req: int, page: int, main_stream, done_event) -> None:

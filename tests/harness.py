@@ -85,10 +85,9 @@ def lru_order_reference(stamp: np.ndarray) -> np.ndarray:
     return np.lexsort((np.arange(stamp.size), stamp)).astype(np.int32)
 
 
-def apply_append_gpu(pool, w, r, page, blk, stream, side, events):
+def write_append_gpu(pool, w, r, page, blk, stream):
     """A finished page: its rows are produced on the GPU (copied in from the
-    generator, standing in for the model writing KV), mapped resident, the
-    context grows, and a host copy is queued on the side stream."""
+    generator, standing in for the model writing KV) and mapped resident."""
     import torch
     import sparse_attention_kv_hs_gb300 as hs
 
@@ -97,6 +96,14 @@ def apply_append_gpu(pool, w, r, page, blk, stream, side, events):
     for l in range(w.L):
         pool.kv_pool[l, blk * w.P:(blk + 1) * w.P].copy_(dev[l])
     hs.hs_map_page(pool.handle, r, page, blk, stream)
+
+
+def apply_append_gpu(pool, w, r, page, blk, stream, side, events):
+    """write_append_gpu, then a host copy of the page queued on the side stream."""
+    import torch
+    import sparse_attention_kv_hs_gb300 as hs
+
+    write_append_gpu(pool, w, r, page, blk, stream)
     ev = torch.cuda.Event()
     hs.hs_offload_prefix(pool.handle, r, page, stream, side, ev)
     events[(r, page)] = ev

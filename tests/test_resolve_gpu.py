@@ -21,7 +21,8 @@ if not torch.cuda.is_available():
 import sparse_attention_kv_hs_gb300 as hs  # noqa: E402
 
 
-def replay(w, *, state_every=1, gather_requests=None, check_offload=True, use_graph=False):
+def replay(w, *, state_every=1, gather_requests=None, check_offload=True, use_graph=False,
+           batch_offload=False):
     scen = W.Scenario.build(w)
     pool = harness.make_pool(w, scen)
     o = harness.make_oracle(w, scen)
@@ -77,8 +78,17 @@ def replay(w, *, state_every=1, gather_requests=None, check_offload=True, use_gr
                     np.testing.assert_array_equal(ss[l, r], stamp_ref)
                     np.testing.assert_array_equal(so[l, r], harness.lru_order_reference(stamp_ref))
         hs.hs_step_advance(pool.step, stream)
+        if batch_offload and scen.appends[t]:  # the step's pages in one offload launch
+            for (r, page, blk) in scen.appends[t]:
+                harness.write_append_gpu(pool, w, r, page, blk, stream)
+            ev = torch.cuda.Event()
+            hs.hs_offload_pages(pool.handle, [a[0] for a in scen.appends[t]],
+                                [a[1] for a in scen.appends[t]], stream, side, ev)
+            for (r, page, blk) in scen.appends[t]:
+                events[(r, page)] = ev
         for (r, page, blk) in scen.appends[t]:
-            harness.apply_append_gpu(pool, w, r, page, blk, stream, side, events)
+            if not batch_offload:
+                harness.apply_append_gpu(pool, w, r, page, blk, stream, side, events)
             ctx[r] += w.P
             hs.hs_set_request(pool.handle, r, int(ctx[r]), int(offs[r]), stream)
             o.set_page(r, page, blk)
@@ -122,6 +132,40 @@ def test_gather_workload_full_size():
 def test_mixed_residency_scaled_down_with_offload():
     w = W.make("mixed", R=16, steps=24, ctx_hi=131072)
     replay(w, state_every=4, gather_requests=lambda t, l: range(w.R) if t % 4 == 0 else [])
+
+
+def test_mixed_residency_scaled_down_with_batched_offload():
+    """The step's appended pages offloaded by one hs_offload_pages launch."""
+    w = W.make("mixed", R=16, steps=24, ctx_hi=131072)
+    replay(w, state_every=4, gather_requests=lambda t, l: range(w.R) if t % 4 == 0 else [],
+           batch_offload=True)
+
+
+def test_offload_pages_arguments_and_unmapped_page():
+    """Out-of-range pairs and counts are rejected with nothing launched; an
+    unmapped page is skipped with error bit BLOCK while the others copy."""
+    w = W.make("tiny")
+    scen = W.Scenario.build(w)
+    pool = harness.make_pool(w, scen)
+    stream, side = torch.cuda.current_stream(), torch.cuda.Stream()
+    ev = torch.cuda.Event()
+    for reqs, pages in ([w.R], [0]), ([0], [-1]), ([0], [10 ** 6]), ([], []), \
+            ([0] * (hs.HS_OFFLOAD_MAX_PAGES + 1), [0] * (hs.HS_OFFLOAD_MAX_PAGES + 1)):
+        with pytest.raises(hs.HsError):
+            hs.hs_offload_pages(pool.handle, reqs, pages, stream, side, ev)
+    blk = pool.blocks_per_layer - 1                        # the resident block
+    last = int(w.ctx_capacity()[0]) // w.P - 1
+    harness.write_append_gpu(pool, w, 0, last, blk, stream)
+    hs.hs_map_page(pool.handle, 0, last - 1, -1, stream)   # unmapped: skipped
+    pool.host_pool[:, int(w.host_offsets()[0]) + last * w.P:][:, :w.P] = 0
+    hs.hs_offload_pages(pool.handle, [0, 0], [last - 1, last], stream, side, ev)
+    torch.cuda.synchronize()
+    assert hs.hs_check_errors(pool.handle) == hs.DEV_ERR_BLOCK
+    base = int(w.host_offsets()[0]) + last * w.P
+    for l in range(w.L):
+        assert np.array_equal(pool.host_pool[l, base:base + w.P],
+                              synth.rows(w.seed, 0, l, last * w.P, w.P))
+    pool.close()
 
 
 def test_mixed_residency_full_size():
