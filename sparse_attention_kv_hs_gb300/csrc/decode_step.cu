@@ -12,15 +12,19 @@
 //
 // Schedule for layers 0 .. n-1 (all selections given):
 //   stream:       RESOLVE(0)  ATTN(0)  [wait R(1)] ATTN(1)  [wait R(2)] ATTN(2) ...
-//   copy_stream:  [wait step start] RESOLVE(1)  RESOLVE(2)  ...
+//   copy_stream:  [wait S] RESOLVE(1)  RESOLVE(2)  ...
 // RESOLVE launches of different layers touch disjoint state (their own
 // slots, position -> slot array and pool rows), so only the data each
-// attention needs orders the two streams.  RESOLVE(1) starts with RESOLVE(0)
-// (on the SMs RESOLVE(0) leaves, then on those its clusters free), so the
-// host link, which bounds RESOLVE, is busy across both launches' start and
-// tail; the attention launches run on the SMs that RESOLVE does not need: a
-// RESOLVE beside another launch takes clusters of 2 CTAs per unit and an
-// attention launch beside a RESOLVE the SMs left.
+// attention needs orders the two streams.  The attention launches run on the
+// SMs that RESOLVE does not need: a RESOLVE beside another launch takes
+// clusters of 2 CTAs per unit and an attention launch beside a RESOLVE the
+// SMs left.  Where the copy stream starts (S):
+//  - bf16 rows (1152 B): with the step.  A RESOLVE launch, bound by the host
+//    link, takes about twice an attention launch; RESOLVE(1) beside RESOLVE(0)
+//    (on the SMs RESOLVE(0) leaves, then on those its clusters free) keeps the
+//    link busy across both launches' start and tail.
+//  - FP8 rows (656 B): after RESOLVE(0).  RESOLVE and attention launches take
+//    about as long as each other, and RESOLVE(1) is best hidden beside ATTN(0).
 #include "hs_internal.cuh"
 
 extern "C" hs_status hs_decode_step(hs_pool* p, int32_t layer_begin, int32_t num_layers,
@@ -69,14 +73,18 @@ extern "C" hs_status hs_decode_step(hs_pool* p, int32_t layer_begin, int32_t num
   if (s_side < 1) s_side = 1;
 
   cudaEvent_t* ev = p->step_events;
-  // copy_stream starts after everything queued on `stream` before this step,
-  // so layer 1's RESOLVE runs beside layer 0's (on the SMs layer 0 leaves, then
-  // on those its clusters free) and the host link stays busy across the two
-  HS_CUDA_TRY(cudaEventRecord(ev[0], s));
-  HS_CUDA_TRY(cudaStreamWaitEvent(cs, ev[0], 0));
+  const bool together = p->d.kv_format == HS_KV_BF16;  // see the schedule above
+  if (together) {  // copy_stream starts after the work queued before this step
+    HS_CUDA_TRY(cudaEventRecord(ev[0], s));
+    HS_CUDA_TRY(cudaStreamWaitEvent(cs, ev[0], 0));
+  }
   if ((st = hs_launch_resolve(p, layer_begin, 1, topk_l(0), d_step, rows_l(0), cnt_l(0), nullptr,
                               0, s)) != HS_OK)
     return st;
+  if (!together) {  // copy_stream starts after RESOLVE(0)
+    HS_CUDA_TRY(cudaEventRecord(ev[0], s));
+    HS_CUDA_TRY(cudaStreamWaitEvent(cs, ev[0], 0));
+  }
   for (int i = 1; i < num_layers; ++i) {
     if ((st = hs_launch_resolve(p, layer_begin + i, 1, topk_l(i), d_step, rows_l(i), cnt_l(i),
                                 nullptr, c_side, cs)) != HS_OK)
