@@ -265,9 +265,11 @@ hs_status hs_sparse_mla_decode(hs_pool* pool, int32_t layer, const void* q,
  *   out          device bf16 [num_layers][R][num_heads][512]
  *   lse          device float [num_layers][R][num_heads] or NULL
  *   miss_count   device int32 [num_layers][R] or NULL
- * `copy_stream` starts after the work queued on `stream` so far, and all of
- * the step's work is ordered before later work on `stream`.  With copy_stream
- * == stream (or one layer) the calls simply run in order on `stream`.
+ * `copy_stream` starts after the work queued on `stream` before the call
+ * (bf16 rows: layer 1's RESOLVE runs beside layer 0's) or, for FP8 rows, after
+ * layer 0's RESOLVE; all of the step's work is ordered before later work on
+ * `stream`.  With copy_stream == stream (or one layer) the calls simply run in
+ * order on `stream`.
  * Attention results may differ from hs_sparse_mla_decode's in the last bits
  * (a launch beside a RESOLVE splits K into fewer parts).  Async,
  * graph-capturable (copy_stream joins the capture through events); uses the
@@ -278,6 +280,29 @@ hs_status hs_decode_step(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
                          int32_t v_dim, float scale, const int32_t* d_step,
                          int32_t* out_row_ids, void* out, float* lse,
                          int32_t* miss_count, void* stream, void* copy_stream);
+
+/* hs_decode_step for a speculative-decoding step: num_tokens (T) verify
+ * tokens per request.  Each layer's RESOLVE takes a unit's T lists as one
+ * (as hs_resolve_tokens), and its attention runs one decode row per
+ * (request, token) (as hs_sparse_mla_decode_tokens); the schedule is
+ * hs_decode_step's.  Page "GLM 5.3 Optimizations, Part 1", section
+ * "Composition with the rest of vLLM": the verify steps share the request's
+ * hot state through a per-step resolver plan that can be replayed.
+ *   topk_idx     device int32 [num_layers][R][T][K]
+ *   q            device bf16 [num_layers][R][T][num_heads][576]
+ *   out_row_ids  device int32 [num_layers][R][T][K]
+ *   out          device bf16 [num_layers][R][T][num_heads][512]
+ *   lse          device float [num_layers][R][T][num_heads] or NULL
+ *   miss_count   device int32 [num_layers][R] or NULL
+ * T = 1 is hs_decode_step.  HS_ERR_INVALID also when R x T > 65535 or the
+ * unit's T x K list does not fit RESOLVE's shared memory (as
+ * hs_resolve_tokens). */
+hs_status hs_decode_step_tokens(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
+                                int32_t num_tokens, const int32_t* topk_idx, const void* q,
+                                int32_t num_heads, int32_t v_dim, float scale,
+                                const int32_t* d_step, int32_t* out_row_ids, void* out,
+                                float* lse, int32_t* miss_count, void* stream,
+                                void* copy_stream);
 
 /* Sparse MLA decode attention of one layer for the T verify tokens of a
  * speculative-decoding step: each (request, token) has its own query and its

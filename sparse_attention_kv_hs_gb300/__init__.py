@@ -43,7 +43,7 @@ EXPORTED = (
     "hs_set_request", "hs_map_page", "hs_load_page", "hs_resolve", "hs_gather",
     "hs_sparse_mla_decode", "hs_offload_prefix", "hs_offload_pages", "hs_commit_offload",
     "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
-    "hs_sparse_mla_decode_noalloc", "hs_decode_step", "hs_resolve_tokens",
+    "hs_sparse_mla_decode_noalloc", "hs_decode_step", "hs_decode_step_tokens", "hs_resolve_tokens",
     "hs_sparse_mla_decode_tokens",
 )
 
@@ -110,6 +110,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_host_read": [p, i64, p, p],
         "hs_sparse_mla_decode_noalloc": [p, i64, p, p, i32, i32, i32, i32, f32, p, p, p],
         "hs_decode_step": [p, i32, i32, p, p, i32, i32, f32, p, p, p, p, p, p, p],
+        "hs_decode_step_tokens": [p, i32, i32, i32, p, p, i32, i32, f32, p, p, p, p, p, p, p],
         "hs_resolve_tokens": [p, i32, i32, i32, p, p, p, p, p, p],
         "hs_sparse_mla_decode_tokens": [p, i32, i32, p, p, i32, i32, f32, p, p, p],
     }
@@ -256,12 +257,23 @@ def hs_sparse_mla_decode_noalloc(kv_rows, num_rows: int, q, row_ids, num_request
 def hs_decode_step(pool: int, layer_begin: int, num_layers: int, topk_idx, q, num_heads: int,
                    v_dim: int, scale: float, d_step, out_row_ids, out, lse=None, miss_count=None,
                    stream=None, copy_stream=None) -> None:
-    """RESOLVE + attention for each layer of one decode step; the next layer's
-    RESOLVE runs on `copy_stream` beside the current layer's attention."""
+    """RESOLVE + attention for each layer of one decode step; the later layers'
+    RESOLVE runs on `copy_stream` beside layer 0's RESOLVE or the attention."""
     _check(load().hs_decode_step(pool, layer_begin, num_layers, _addr(topk_idx), _addr(q),
                                  num_heads, v_dim, scale, _addr(d_step), _addr(out_row_ids),
                                  _addr(out), _addr(lse), _addr(miss_count), _stream(stream),
                                  _stream(copy_stream)), "hs_decode_step")
+
+
+def hs_decode_step_tokens(pool: int, layer_begin: int, num_layers: int, num_tokens: int, topk_idx,
+                          q, num_heads: int, v_dim: int, scale: float, d_step, out_row_ids, out,
+                          lse=None, miss_count=None, stream=None, copy_stream=None) -> None:
+    """hs_decode_step over num_tokens verify tokens per request."""
+    _check(load().hs_decode_step_tokens(pool, layer_begin, num_layers, num_tokens,
+                                        _addr(topk_idx), _addr(q), num_heads, v_dim, scale,
+                                        _addr(d_step), _addr(out_row_ids), _addr(out), _addr(lse),
+                                        _addr(miss_count), _stream(stream), _stream(copy_stream)),
+           "hs_decode_step_tokens")
 
 
 def hs_offload_prefix(pool: int, req: int, page: int, main_stream, side_stream, done_event) -> None:

@@ -27,12 +27,17 @@
 //    about as long as each other, and RESOLVE(1) is best hidden beside ATTN(0).
 #include "hs_internal.cuh"
 
-extern "C" hs_status hs_decode_step(hs_pool* p, int32_t layer_begin, int32_t num_layers,
-                                    const int32_t* topk_idx, const void* q, int32_t num_heads,
-                                    int32_t v_dim, float scale, const int32_t* d_step,
-                                    int32_t* out_row_ids, void* out, float* lse,
-                                    int32_t* miss_count, void* stream, void* copy_stream) {
-  if (!p || !topk_idx || !q || !d_step || !out_row_ids || !out) return HS_ERR_INVALID;
+// num_tokens verify tokens per request (speculative decoding; 1 otherwise):
+// each layer's RESOLVE takes a unit's T lists as one (hs_resolve_tokens) and
+// its attention runs one decode row per (request, token).
+extern "C" hs_status hs_decode_step_tokens(hs_pool* p, int32_t layer_begin, int32_t num_layers,
+                                           int32_t num_tokens, const int32_t* topk_idx,
+                                           const void* q, int32_t num_heads, int32_t v_dim,
+                                           float scale, const int32_t* d_step,
+                                           int32_t* out_row_ids, void* out, float* lse,
+                                           int32_t* miss_count, void* stream, void* copy_stream) {
+  if (!p || !topk_idx || !q || !d_step || !out_row_ids || !out || num_tokens <= 0)
+    return HS_ERR_INVALID;
   if (num_layers <= 0 || layer_begin < 0 || layer_begin + num_layers > p->d.num_layers)
     return HS_ERR_INVALID;
   // the attention launches' own checks, made before anything is queued
@@ -41,35 +46,40 @@ extern "C" hs_status hs_decode_step(hs_pool* p, int32_t layer_begin, int32_t num
     return HS_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
     return HS_ERR_INVALID;
-  const int64_t R = p->d.num_requests, K = p->d.top_k, H = num_heads;
+  const int64_t R = p->d.num_requests, K = p->d.top_k, H = num_heads, T = num_tokens;
   const int64_t D = p->d.row_elems;
-  auto topk_l = [&](int i) { return topk_idx + i * R * K; };
-  auto rows_l = [&](int i) { return out_row_ids + i * R * K; };
+  if (R * T > 65535) return HS_ERR_INVALID;
+  auto topk_l = [&](int i) { return topk_idx + i * R * T * K; };
+  auto rows_l = [&](int i) { return out_row_ids + i * R * T * K; };
   auto cnt_l = [&](int i) { return miss_count ? miss_count + i * R : nullptr; };
-  auto q_l = [&](int i) { return static_cast<const char*>(q) + i * R * H * D * 2; };
-  auto out_l = [&](int i) { return static_cast<char*>(out) + i * R * H * v_dim * 2; };
-  auto lse_l = [&](int i) { return lse ? lse + i * R * H : nullptr; };
+  auto q_l = [&](int i) { return static_cast<const char*>(q) + i * R * T * H * D * 2; };
+  auto out_l = [&](int i) { return static_cast<char*>(out) + i * R * T * H * v_dim * 2; };
+  auto lse_l = [&](int i) { return lse ? lse + i * R * T * H : nullptr; };
+  auto resolve = [&](int i, int max_cluster, cudaStream_t st) {
+    return hs_launch_resolve_tokens(p, layer_begin + i, 1, num_tokens, topk_l(i), d_step,
+                                    rows_l(i), cnt_l(i), nullptr, max_cluster, st);
+  };
+  auto attention = [&](int i, int max_splits, cudaStream_t st) {
+    return hs_launch_attention_tokens(p, layer_begin + i, num_tokens, q_l(i), rows_l(i), num_heads,
+                                      v_dim, scale, out_l(i), lse_l(i), max_splits, st);
+  };
   cudaStream_t s = hs_stream(stream), cs = hs_stream(copy_stream);
 
   hs_status st;
   if (cs == s || num_layers == 1) {  // one stream: the plain sequence
     for (int i = 0; i < num_layers; ++i) {
-      if ((st = hs_launch_resolve(p, layer_begin + i, 1, topk_l(i), d_step, rows_l(i), cnt_l(i),
-                                  nullptr, 0, s)) != HS_OK)
-        return st;
-      if ((st = hs_launch_attention(p, layer_begin + i, q_l(i), rows_l(i), num_heads, v_dim, scale,
-                                    out_l(i), lse_l(i), 0, s)) != HS_OK)
-        return st;
+      if ((st = resolve(i, 0, s)) != HS_OK) return st;
+      if ((st = attention(i, 0, s)) != HS_OK) return st;
     }
     return HS_OK;
   }
 
   // SMs while a RESOLVE runs beside an attention launch: RESOLVE clusters of
   // 2 CTAs per unit (1 if that leaves too few), attention the splits that fit
-  // in the rest (at least one CTA pair per request)
+  // in the rest (at least one CTA pair per decode row)
   const int64_t sms = p->num_sms;
   const int c_side = 3 * R <= sms ? 2 : 1;
-  int s_side = (int)((sms - c_side * R) / (2 * R));
+  int s_side = (int)((sms - c_side * R) / (2 * R * T));
   if (s_side < 1) s_side = 1;
 
   cudaEvent_t* ev = p->step_events;
@@ -78,25 +88,27 @@ extern "C" hs_status hs_decode_step(hs_pool* p, int32_t layer_begin, int32_t num
     HS_CUDA_TRY(cudaEventRecord(ev[0], s));
     HS_CUDA_TRY(cudaStreamWaitEvent(cs, ev[0], 0));
   }
-  if ((st = hs_launch_resolve(p, layer_begin, 1, topk_l(0), d_step, rows_l(0), cnt_l(0), nullptr,
-                              0, s)) != HS_OK)
-    return st;
+  if ((st = resolve(0, 0, s)) != HS_OK) return st;
   if (!together) {  // copy_stream starts after RESOLVE(0)
     HS_CUDA_TRY(cudaEventRecord(ev[0], s));
     HS_CUDA_TRY(cudaStreamWaitEvent(cs, ev[0], 0));
   }
   for (int i = 1; i < num_layers; ++i) {
-    if ((st = hs_launch_resolve(p, layer_begin + i, 1, topk_l(i), d_step, rows_l(i), cnt_l(i),
-                                nullptr, c_side, cs)) != HS_OK)
-      return st;
+    if ((st = resolve(i, c_side, cs)) != HS_OK) return st;
     HS_CUDA_TRY(cudaEventRecord(ev[i], cs));
   }
   for (int i = 0; i < num_layers; ++i) {
     if (i > 0) HS_CUDA_TRY(cudaStreamWaitEvent(s, ev[i], 0));
-    if ((st = hs_launch_attention(p, layer_begin + i, q_l(i), rows_l(i), num_heads, v_dim, scale,
-                                  out_l(i), lse_l(i), i + 1 < num_layers ? s_side : 0, s)) !=
-        HS_OK)
-      return st;
+    if ((st = attention(i, i + 1 < num_layers ? s_side : 0, s)) != HS_OK) return st;
   }
   return HS_OK;
+}
+
+extern "C" hs_status hs_decode_step(hs_pool* p, int32_t layer_begin, int32_t num_layers,
+                                    const int32_t* topk_idx, const void* q, int32_t num_heads,
+                                    int32_t v_dim, float scale, const int32_t* d_step,
+                                    int32_t* out_row_ids, void* out, float* lse,
+                                    int32_t* miss_count, void* stream, void* copy_stream) {
+  return hs_decode_step_tokens(p, layer_begin, num_layers, 1, topk_idx, q, num_heads, v_dim, scale,
+                               d_step, out_row_ids, out, lse, miss_count, stream, copy_stream);
 }

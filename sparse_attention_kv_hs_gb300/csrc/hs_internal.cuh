@@ -64,12 +64,24 @@ hs_status hs_launch_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_laye
                             const int32_t* topk, const int32_t* d_step, int32_t* out_rows,
                             int32_t* miss_count, int32_t* miss_log, int max_cluster,
                             cudaStream_t stream);
+// RESOLVE of num_tokens verify tokens per unit, taken as one list (as
+// hs_resolve_tokens).
+hs_status hs_launch_resolve_tokens(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
+                                   int32_t num_tokens, const int32_t* topk, const int32_t* d_step,
+                                   int32_t* out_rows, int32_t* miss_count, int32_t* miss_log,
+                                   int max_cluster, cudaStream_t stream);
 // Sparse MLA decode of one layer (arguments as hs_sparse_mla_decode);
 // max_splits > 0 caps the K splits per request (fewer SMs), 0 = the pool's.
 hs_status hs_launch_attention(hs_pool* pool, int32_t layer, const void* q,
                               const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
                               float scale, void* out, float* lse, int max_splits,
                               cudaStream_t stream);
+// The same over the num_tokens verify tokens of each request (q, row_ids, out
+// and lse laid out as for hs_sparse_mla_decode_tokens).
+hs_status hs_launch_attention_tokens(hs_pool* pool, int32_t layer, int32_t num_tokens,
+                                     const void* q, const int32_t* row_ids, int32_t num_heads,
+                                     int32_t v_dim, float scale, void* out, float* lse,
+                                     int max_splits, cudaStream_t stream);
 hs_status hs_attn_workspace_init(hs_pool* pool);
 void hs_attn_workspace_free(hs_pool* pool);
 // Shared memory the RESOLVE kernel needs for these sizes; sets the kernel's

@@ -1269,55 +1269,15 @@ void hs_attn_workspace_free(hs_pool* p) {
   p->attn_kv_maps = nullptr;
 }
 
-hs_status hs_launch_attention(hs_pool* p, int32_t layer, const void* q, const int32_t* row_ids,
-                              int32_t num_heads, int32_t v_dim, float scale, void* out, float* lse,
-                              int max_splits, cudaStream_t stream) {
-  if (!p || !q || !row_ids || !out) return HS_ERR_INVALID;
-  if (layer < 0 || layer >= p->d.num_layers || num_heads <= 0 || num_heads > kHeads ||
-      v_dim != kDV || p->d.row_elems != kD || !(scale > 0.f) || p->attn_max_splits < 1 ||
-      !p->attn_kv_maps)
-    return HS_ERR_INVALID;
-  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
-    return HS_ERR_INVALID;
-  const int64_t rows_in_layer = p->blocks_per_layer * p->d.page_tokens;
-  if (rows_in_layer > INT32_MAX) return HS_ERR_INVALID;
-  AttnArgs a;
-  a.kv = layer_rows(p, layer, rows_in_layer);
-  a.row_ids = row_ids;
-  a.out = static_cast<uint16_t*>(out);
-  a.lse = lse;
-  a.ws_o = p->attn_o;
-  a.ws_lse = p->attn_ml;
-  a.error_word = p->error_word;
-  a.rows_in_layer = (int32_t)rows_in_layer;
-  a.K = p->d.top_k;
-  a.H = num_heads;
-  a.splits = p->attn_max_splits;
-  if (max_splits > 0 && max_splits < a.splits) {
-    const int tiles = (a.K + kTile - 1) / kTile;
-    const int min_splits = (tiles * kTile + kMaxSplitRows - 1) / kMaxSplitRows;
-    a.splits = max_splits > min_splits ? max_splits : min_splits;
-  }
-  a.scale_log2 = scale * 1.4426950408889634f;
-  return launch_decode(a, static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q,
-                       p->d.num_requests, stream, p->d.kv_format == HS_KV_FP8);
-}
-
-extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void* q,
-                                          const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
-                                          float scale, void* out, float* lse, void* stream) {
-  return hs_launch_attention(p, layer, q, row_ids, num_heads, v_dim, scale, out, lse, 0,
-                             hs_stream(stream));
-}
-
-// Speculative decoding: each request's T verify tokens have their own query and
-// their own K rows (hs_resolve_tokens' output), so the T tokens of R requests
-// are R * T independent decode rows of the same kernel.  Their K splits are
-// capped so that the partials fit the pool's workspace (R x its splits).
-extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int32_t num_tokens,
-                                                 const void* q, const int32_t* row_ids,
-                                                 int32_t num_heads, int32_t v_dim, float scale,
-                                                 void* out, float* lse, void* stream) {
+// Decode rows of one layer: the T verify tokens of R requests are R * T
+// independent decode rows of the same kernel (T = 1 outside speculative
+// decoding), each with its own query and its own K rows.  Their K splits are
+// the kernel's choice for R * T rows, capped so that the partials fit the
+// pool's workspace (R x its splits) and, if max_splits > 0, at max_splits.
+hs_status hs_launch_attention_tokens(hs_pool* p, int32_t layer, int32_t num_tokens, const void* q,
+                                     const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
+                                     float scale, void* out, float* lse, int max_splits,
+                                     cudaStream_t stream) {
   if (!p || !q || !row_ids || !out || num_tokens <= 0) return HS_ERR_INVALID;
   if (layer < 0 || layer >= p->d.num_layers || num_heads <= 0 || num_heads > kHeads ||
       v_dim != kDV || p->d.row_elems != kD || !(scale > 0.f) || p->attn_max_splits < 1 ||
@@ -1333,6 +1293,7 @@ extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int3
   int splits = choose_splits(p->num_sms, (int)n, p->d.top_k);
   const int fit = p->attn_max_splits / num_tokens;  // partials the workspace holds per row
   if (splits > 1 && splits > fit) splits = fit > min_splits ? fit : min_splits;
+  if (max_splits > 0 && max_splits < splits) splits = max_splits > min_splits ? max_splits : min_splits;
   if (splits > 1 && n * splits > (int64_t)p->d.num_requests * p->attn_max_splits)
     return HS_ERR_INVALID;  // K too long for this many rows in the workspace
   AttnArgs a;
@@ -1349,7 +1310,29 @@ extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int3
   a.splits = splits;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_decode(a, static_cast<const CUtensorMap*>(p->attn_kv_maps)[layer], q, (int)n,
-                       hs_stream(stream), p->d.kv_format == HS_KV_FP8);
+                       stream, p->d.kv_format == HS_KV_FP8);
+}
+
+hs_status hs_launch_attention(hs_pool* p, int32_t layer, const void* q, const int32_t* row_ids,
+                              int32_t num_heads, int32_t v_dim, float scale, void* out, float* lse,
+                              int max_splits, cudaStream_t stream) {
+  return hs_launch_attention_tokens(p, layer, 1, q, row_ids, num_heads, v_dim, scale, out, lse,
+                                    max_splits, stream);
+}
+
+extern "C" hs_status hs_sparse_mla_decode(hs_pool* p, int32_t layer, const void* q,
+                                          const int32_t* row_ids, int32_t num_heads, int32_t v_dim,
+                                          float scale, void* out, float* lse, void* stream) {
+  return hs_launch_attention(p, layer, q, row_ids, num_heads, v_dim, scale, out, lse, 0,
+                             hs_stream(stream));
+}
+
+extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int32_t num_tokens,
+                                                 const void* q, const int32_t* row_ids,
+                                                 int32_t num_heads, int32_t v_dim, float scale,
+                                                 void* out, float* lse, void* stream) {
+  return hs_launch_attention_tokens(p, layer, num_tokens, q, row_ids, num_heads, v_dim, scale, out,
+                                    lse, 0, hs_stream(stream));
 }
 
 // ---------------------------------------------------------------------------

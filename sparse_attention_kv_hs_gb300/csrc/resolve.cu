@@ -775,6 +775,14 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
                         miss_log, max_cluster, stream);
 }
 
+hs_status hs_launch_resolve_tokens(hs_pool* p, int32_t layer_begin, int32_t num_layers,
+                                   int32_t num_tokens, const int32_t* topk, const int32_t* d_step,
+                                   int32_t* out_rows, int32_t* miss_count, int32_t* miss_log,
+                                   int max_cluster, cudaStream_t stream) {
+  return launch_resolve(p, layer_begin, num_layers, num_tokens, topk, d_step, out_rows,
+                        miss_count, miss_log, max_cluster, stream);
+}
+
 extern "C" hs_status hs_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
                                 const int32_t* topk_idx, const int32_t* d_step,
                                 int32_t* out_row_ids, int32_t* miss_count, int32_t* miss_log,

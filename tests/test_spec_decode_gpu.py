@@ -152,3 +152,64 @@ def test_lists_too_large_for_one_cta_are_rejected():
     with pytest.raises(hs.HsError):
         hs.hs_resolve_tokens(pool.handle, 0, 1, 4, t, pool.step, t.clone())
     pool.close()
+
+
+def replay_step_tokens(w, check_steps, attn_requests, same_stream=False, kv_format=0):
+    """hs_decode_step_tokens over every layer of each step against the oracle."""
+    scen = W.Scenario.build(w)
+    pool = harness.make_pool(w, scen, kv_format)
+    o = harness.make_oracle(w, scen)
+    R, L, K, T, H = w.R, w.L, w.K, w.tokens, w.heads
+    tr = np.stack([w.trace_tokens(r) for r in range(R)], axis=2)  # [steps][L][R][T][K]
+    d_topk = torch.empty((L, R, T, K), dtype=torch.int32, device="cuda")
+    d_rows = torch.empty((L, R, T, K), dtype=torch.int32, device="cuda")
+    d_cnt = torch.empty((L, R), dtype=torch.int32, device="cuda")
+    d_q = torch.empty((L, R, T, H, W.ROW_ELEMS), dtype=torch.int16, device="cuda")
+    d_o = torch.empty((L, R, T, H, W.V_DIM), dtype=torch.bfloat16, device="cuda")
+    d_lse = torch.empty((L, R, T, H), dtype=torch.float32, device="cuda")
+    main = torch.cuda.Stream()
+    copy = main if same_stream else torch.cuda.Stream()
+    for t in range(w.steps):
+        q = np.stack([np.stack([np.stack([synth.q(w.seed, r, l, t * T + k, H) for k in range(T)])
+                                for r in range(R)]) for l in range(L)])
+        d_topk.copy_(torch.from_numpy(tr[t]))
+        d_q.copy_(torch.from_numpy(q.view(np.int16)))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(main):
+            hs.hs_decode_step_tokens(pool.handle, 0, L, T, d_topk, d_q, H, W.V_DIM, W.SCALE,
+                                     pool.step, d_rows, d_o, d_lse, d_cnt, main, copy)
+            hs.hs_step_advance(pool.step, main)
+        torch.cuda.synchronize()
+        rows, cnt = d_rows.cpu().numpy(), d_cnt.cpu().numpy()
+        out, lse = d_o.float().cpu().numpy(), d_lse.cpu().numpy()
+        for l in range(L):
+            for r in range(R):
+                ref_rows, ref_log, err = o.resolve_tokens(l, r, tr[t, l, r], t)
+                assert err == 0
+                np.testing.assert_array_equal(rows[l, r], ref_rows, err_msg=f"t={t} l={l} r={r}")
+                assert cnt[l, r] == len(ref_log), (t, l, r)
+                if t in check_steps and r in attn_requests:
+                    for k in range(T):
+                        kv = harness.rows_for_oracle(w, r, l, tr[t, l, r, k], kv_format)
+                        ref, ref_lse = oracle.sparse_mla_decode(q[l, r, k], kv, None, W.SCALE)
+                        _check(out[l, r, k], ref, (t, l, r, k))
+                        assert np.allclose(lse[l, r, k], ref_lse, rtol=0, atol=2e-3)
+    assert hs.hs_check_errors(pool.handle) == 0
+    pool.close()
+
+
+def test_decode_step_tokens_spec_workload_full_size():
+    """32 requests x 2 layers, T = 2, K 2048, B 8192: the spec benchmark's step,
+    layer 1's RESOLVE on the copy stream."""
+    w = W.make("spec", steps=6)
+    replay_step_tokens(w, check_steps={0, 5}, attn_requests={0, 9, 31})
+
+
+def test_decode_step_tokens_on_one_stream_scaled_down():
+    w = W.make("spec", R=4, steps=4)
+    replay_step_tokens(w, check_steps={0, 3}, attn_requests=set(range(4)), same_stream=True)
+
+
+def test_decode_step_tokens_fp8_rows():
+    w = W.make("spec", R=4, steps=4)
+    replay_step_tokens(w, check_steps={0, 3}, attn_requests=set(range(4)), kv_format=1)
