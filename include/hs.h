@@ -198,8 +198,9 @@ hs_status hs_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
  *   miss_count   device int32 [num_layers][R] or NULL: misses served
  *   miss_log     device int32 [num_layers][R][T*K][3] or NULL: (j, position,
  *                slot) per served miss, j indexing the unit's T*K list
- * Size limit: the unit's tables for T*K entries and B slots must fit one
- * CTA's shared memory (e.g. T = 2 at K = 2048, B = 8192); otherwise
+ * Size limit: at most 8192 entries (T*K) per unit, and the unit's tables for
+ * them and B slots must fit one CTA's shared memory (T = 4 at K = 2048 with
+ * B up to 12288, when the page table has at most 4096 pages); otherwise
  * HS_ERR_INVALID.  Async, graph-capturable, no allocation. */
 hs_status hs_resolve_tokens(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
                             int32_t num_tokens, const int32_t* topk_idx,

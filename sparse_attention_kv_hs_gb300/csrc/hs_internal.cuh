@@ -87,4 +87,5 @@ void hs_attn_workspace_free(hs_pool* pool);
 // Shared memory the RESOLVE kernel needs for these sizes; sets the kernel's
 // dynamic shared-memory limit (call once per pool, outside stream capture).
 // Also reports how many RESOLVE clusters of 1, 2, 4 and 8 CTAs fit at once.
-hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes, int max_clusters[4]);
+hs_status hs_resolve_configure(int K, int B, int P, int max_pages, size_t* smem_bytes,
+                               int max_clusters[4]);

@@ -145,7 +145,7 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
   const int64_t R = d.num_requests, L = d.num_layers, B = d.hot_slots;
   {
     size_t smem = 0;
-    if ((st = hs_resolve_configure(d.top_k, d.hot_slots, d.page_tokens, &smem,
+    if ((st = hs_resolve_configure(d.top_k, d.hot_slots, d.page_tokens, d.max_pages, &smem,
                                    p->resolve_max_clusters)) != HS_OK) {
       delete p;
       return st;

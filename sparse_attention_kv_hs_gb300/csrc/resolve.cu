@@ -71,27 +71,27 @@ struct ResolveArgs {
 // Both layouts start with one mbarrier at offset 0, so each CTA of a cluster
 // can address its peers' barrier without knowing their layout.
 struct SmemPlan {
-  size_t bar, order, sel_key, sel_j, miss_j, miss_p, victim, hot, flag, warp, ptab, alias, total;
+  size_t bar, order, sel, miss_j, miss_p, victim, hot, flag, warp, ptab, alias, total;
 };
 
 constexpr int kMaxSmemPages = 4096;  // page-table rows up to this width are staged in smem
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int sel_bits) {
+// ptab_pages: page-table entries staged (min(max_pages, kMaxSmemPages)).
+__host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int sel_bits, int ptab_pages) {
   SmemPlan s;
   size_t o = 0;
   s.bar = o;       o = 16;
   s.order = o;     o = align16(o + sizeof(int32_t) * B);
-  s.sel_key = o;   o = align16(o + sizeof(int32_t) * (size_t(1) << sel_bits));
-  s.sel_j = o;     o = align16(o + sizeof(int32_t) * (size_t(1) << sel_bits));
+  s.sel = o;       o = align16(o + sizeof(int32_t) * (size_t(1) << sel_bits));
   s.miss_j = o;    o = align16(o + sizeof(int32_t) * K);
   s.miss_p = o;    o = align16(o + sizeof(int32_t) * K);
   s.victim = o;    o = align16(o + sizeof(int32_t) * K);
   s.hot = o;       o = align16(o + sizeof(int32_t) * (B / P));
   s.flag = o;      o = align16(o + B);
   s.warp = o;      o = align16(o + sizeof(int32_t) * (kWarps + 8));
-  s.ptab = o;      o = align16(o + sizeof(int32_t) * kMaxSmemPages);
+  s.ptab = o;      o = align16(o + sizeof(int32_t) * ptab_pages);
   s.alias = o;     o = align16(o + sizeof(uint32_t) * kThreads);
   s.total = o;
   return s;
@@ -102,7 +102,7 @@ __host__ __device__ inline SmemPlan smem_plan(int K, int B, int P, int sel_bits)
 // With several verify tokens (dedup_bits > 0) a fetch CTA also holds its own
 // selection hash, so that a position several tokens select is fetched once.
 struct FetchPlan {
-  size_t bar, j, p, dst, warp, sel_key, sel_j, stage;
+  size_t bar, j, p, dst, warp, sel, stage;
 };
 
 __host__ __device__ inline FetchPlan fetch_plan(int S, int dedup_bits) {
@@ -114,8 +114,7 @@ __host__ __device__ inline FetchPlan fetch_plan(int S, int dedup_bits) {
   f.dst = o;   o = align16(o + sizeof(int32_t) * S);
   f.warp = o;  o = align16(o + sizeof(int32_t) * (kWarps + 8));
   const size_t hash = dedup_bits > 0 ? sizeof(int32_t) * (size_t(1) << dedup_bits) : 0;
-  f.sel_key = o;  o = align16(o + hash);
-  f.sel_j = o;    o = align16(o + hash);
+  f.sel = o;   o = align16(o + hash);
   f.stage = o;
   return f;
 }
@@ -151,25 +150,34 @@ __device__ __forceinline__ uint32_t hash_pos(int32_t p, int bits) {
 
 // Selection hash in shared memory (open addressing, linear probing; key -1 =
 // empty): position -> the smallest list index j that selects it.
-__device__ __forceinline__ void sel_insert(int32_t* key, int32_t* first, int bits, int32_t p,
-                                           int j) {
+// Selection hash over a list (open addressing, linear probing): a slot holds
+// the first index j of the list whose entry is the slot's position, or -1;
+// the position itself is read back from the list.  Inserts may run
+// concurrently; lookups run after every insert.
+__device__ __forceinline__ void sel_insert(int32_t* slot, int bits, int32_t p, int j,
+                                           const int32_t* list) {
   const int mask = (1 << bits) - 1;
   uint32_t h = hash_pos(p, bits);
   for (int probe = 0; probe <= mask; ++probe) {
-    const int32_t prev = atomicCAS(&key[h], -1, p);
-    if (prev == -1 || prev == p) {
-      atomicMin(&first[h], j);
+    const int32_t prev = atomicCAS(&slot[h], -1, j);
+    if (prev == -1) return;
+    if (__ldg(list + prev) == p) {  // p's slot: keep the smallest j
+      atomicMin(&slot[h], j);
       return;
     }
     h = (h + 1) & mask;
   }
 }
-__device__ __forceinline__ int32_t sel_first(const int32_t* key, const int32_t* first, int bits,
-                                             int32_t p) {
+// The first j whose entry is p, or -1.  `hint`: an index known to hold p (no
+// list read when the slot holds it), or -1.
+__device__ __forceinline__ int32_t sel_first(const int32_t* slot, int bits, int32_t p,
+                                             const int32_t* list, int hint) {
   const int mask = (1 << bits) - 1;
   uint32_t h = hash_pos(p, bits);
   for (int probe = 0; probe <= mask; ++probe) {
-    if (key[h] == p) return first[h];
+    const int32_t v = slot[h];
+    if (v < 0) return -1;
+    if (v == hint || __ldg(list + v) == p) return v;
     h = (h + 1) & mask;
   }
   return -1;
@@ -335,17 +343,13 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     int* s_warp = reinterpret_cast<int*>(smem + fp.warp);
     const int cap = (int)((a.smem_bytes - (int64_t)fp.stage) / row_bytes);
 
-    int32_t* f_key = reinterpret_cast<int32_t*>(smem + fp.sel_key);
-    int32_t* f_first = reinterpret_cast<int32_t*>(smem + fp.sel_j);
+    int32_t* f_sel = reinterpret_cast<int32_t*>(smem + fp.sel);
     if (dedup) {  // the whole list's selection hash, as CTA 0 builds it
-      for (int h = tid; h < (1 << a.sel_bits); h += kThreads) {
-        f_key[h] = -1;
-        f_first[h] = INT32_MAX;
-      }
+      for (int h = tid; h < (1 << a.sel_bits); h += kThreads) f_sel[h] = -1;
       __syncthreads();
       for (int j = tid; j < K; j += kThreads) {
         const int32_t p = topk[j];
-        if (p >= 0 && p < ctx) sel_insert(f_key, f_first, a.sel_bits, p, j);
+        if (p >= 0 && p < ctx) sel_insert(f_sel, a.sel_bits, p, j, topk);
       }
       __syncthreads();
     }
@@ -368,7 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     }
     if (dedup) {  // a position an earlier entry selected is fetched for that entry only
       for (int q = 0; q < kptf; ++q)  // (topk re-read: no array indexed at run time)
-        if ((miss_mask >> q) & 1u && sel_first(f_key, f_first, a.sel_bits, topk[j0 + q]) != j0 + q)
+        if ((miss_mask >> q) & 1u &&
+            sel_first(f_sel, a.sel_bits, topk[j0 + q], topk, j0 + q) != j0 + q)
           miss_mask &= ~(1u << q);
     }
     int n_local;
@@ -404,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   }
 
   // ======================= metadata CTA =======================
-  const SmemPlan sp = smem_plan(a.K, a.B, a.P, a.sel_bits);
+  const bool ptab_in_smem = a.max_pages <= kMaxSmemPages;
+  const SmemPlan sp = smem_plan(a.K, a.B, a.P, a.sel_bits, ptab_in_smem ? a.max_pages : 0);
   int32_t* s_order = reinterpret_cast<int32_t*>(smem + sp.order);
-  int32_t* s_sel_key = reinterpret_cast<int32_t*>(smem + sp.sel_key);
-  int32_t* s_sel_j = reinterpret_cast<int32_t*>(smem + sp.sel_j);
+  int32_t* s_sel = reinterpret_cast<int32_t*>(smem + sp.sel);
   int32_t* s_miss_j = reinterpret_cast<int32_t*>(smem + sp.miss_j);
   int32_t* s_miss_p = reinterpret_cast<int32_t*>(smem + sp.miss_p);
   int32_t* s_victim = reinterpret_cast<int32_t*>(smem + sp.victim);
@@ -431,13 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     s_order[s] = g_order[s];
     s_flag[s] = 0;
   }
-  for (int h = tid; h <= sel_mask; h += kThreads) {
-    s_sel_key[h] = -1;
-    s_sel_j[h] = INT32_MAX;
-  }
+  for (int h = tid; h <= sel_mask; h += kThreads) s_sel[h] = -1;
   for (int i = tid; i < hot_per_req; i += kThreads)
     s_hot[i] = a.hot_block[(int64_t)r * hot_per_req + i];
-  const bool ptab_in_smem = a.max_pages <= kMaxSmemPages;
   if (ptab_in_smem)
     for (int i = tid; i < a.max_pages; i += kThreads) s_ptab[i] = ptab[i];
   __syncthreads();
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     my_p[q] = (q < a.kpt && j < K) ? topk[j] : -1;
     const int32_t p = my_p[q];
     if (q >= a.kpt || j >= K || p < 0 || p >= ctx) continue;
-    sel_insert(s_sel_key, s_sel_j, a.sel_bits, p, j);
+    sel_insert(s_sel, a.sel_bits, p, j, topk);
   }
   __syncthreads();
 
@@ -474,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       continue;
     }
     {  // first occurrence of p in the list?
-      const int32_t first = sel_first(s_sel_key, s_sel_j, a.sel_bits, p);
+      const int32_t first = sel_first(s_sel, a.sel_bits, p, topk, j);
       if (first != j) {
         if (first / a.ktok == j / a.ktok) {  // a repeat within one token's row
           err |= HS_DEV_ERR_DUPLICATE;
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     for (int q = 0; q < 8; ++q)
       if (alias_mask & (1u << q)) {
         const int j = j0 + q;
-        out[j] = __ldcg(out + sel_first(s_sel_key, s_sel_j, a.sel_bits, topk[j]));
+        out[j] = __ldcg(out + sel_first(s_sel, a.sel_bits, topk[j], topk, -1));
       }
   }
 
@@ -641,9 +642,11 @@ int ceil_log2(int64_t x) {
 
 }  // namespace
 
-hs_status hs_resolve_configure(int K, int B, int P, size_t* smem_bytes, int max_clusters[4]) {
+hs_status hs_resolve_configure(int K, int B, int P, int max_pages, size_t* smem_bytes,
+                               int max_clusters[4]) {
   const int sel_bits = ceil_log2(2 * (int64_t)K) < 5 ? 5 : ceil_log2(2 * (int64_t)K);
-  const size_t tables = smem_plan(K, B, P, sel_bits).total;
+  const size_t tables =
+      smem_plan(K, B, P, sel_bits, max_pages <= kMaxSmemPages ? max_pages : 0).total;
   int dev = 0, optin = 0;
   HS_CUDA_TRY(cudaGetDevice(&dev));
   HS_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
@@ -729,7 +732,8 @@ hs_status launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers, in
   // The kernel's dynamic shared-memory limit was raised by hs_pool_create
   // (hs_resolve_configure): nothing here may call outside the stream.
   const size_t smem = p->resolve_smem;
-  if (num_tokens > 1 && (smem_plan(a.K, a.B, a.P, a.sel_bits).total > smem ||
+  const int ptab_pages = a.max_pages <= kMaxSmemPages ? a.max_pages : 0;
+  if (num_tokens > 1 && (smem_plan(a.K, a.B, a.P, a.sel_bits, ptab_pages).total > smem ||
                          fetch_plan(a.K, a.sel_bits).stage > smem))
     return HS_ERR_INVALID;  // the list's tables do not fit one CTA's shared memory
   a.smem_bytes = (int32_t)smem;

@@ -207,8 +207,10 @@ def _log_uniform_ctx(R: int, lo: int, hi: int, seed: int, budget_bytes: int, L: 
 
 
 def make(name: str, *, R: int | None = None, steps: int | None = None,
-         ctx: int | None = None, ctx_hi: int | None = None, L: int | None = None) -> Workload:
-    """One of the five workloads; keyword overrides give scaled-down copies."""
+         ctx: int | None = None, ctx_hi: int | None = None, L: int | None = None,
+         tokens: int | None = None) -> Workload:
+    """One of the workloads; keyword overrides give scaled-down copies (tokens:
+    the spec workload's verify tokens T, with B = (T + 2) K)."""
     if name == "tiny":
         R_ = R or 1
         w = Workload("tiny", R_, L or 1, 256, 512, steps or 64,
@@ -231,7 +233,7 @@ def make(name: str, *, R: int | None = None, steps: int | None = None,
                      0.7, 0.0, 0.0, 128, 1004)
     elif name == "spec":
         R_ = R or 32
-        T = 2
+        T = tokens or 2
         w = Workload("spec", R_, L or 2, 2048, (T + 2) * 2048, steps or 64,
                      np.full(R_, ctx or 65536, dtype=np.int64), 0, ["zero"] * R_,
                      0.7, 0.0, 0.0, 128, 1006, tokens=T, token_share=0.85)

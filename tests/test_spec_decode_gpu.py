@@ -146,12 +146,27 @@ def test_repeats_within_and_across_tokens():
 
 
 def test_lists_too_large_for_one_cta_are_rejected():
-    """T = 4 tokens of K 2048 with B = 6 K: the unit's tables exceed one CTA."""
-    pool = hs.Pool(1, 1, 2048, 6 * 2048, 256, W.ROW_ELEMS, 256, 65536, 1)
-    t = torch.zeros((1, 4, 2048), dtype=torch.int32, device="cuda")
-    with pytest.raises(hs.HsError):
-        hs.hs_resolve_tokens(pool.handle, 0, 1, 4, t, pool.step, t.clone())
-    pool.close()
+    """T = 5 tokens of K 2048 (10,240 entries, more than one CTA's 8,192) and
+    T = 4 with B = 12,800 (the tables of 8,192 entries exceed one CTA's shared
+    memory; B = 12,288 fits)."""
+    for T, B in ((5, 7 * 2048), (4, 50 * 256)):
+        pool = hs.Pool(1, 1, 2048, B, 256, W.ROW_ELEMS, 256, 65536, 1)
+        t = torch.zeros((1, T, 2048), dtype=torch.int32, device="cuda")
+        with pytest.raises(hs.HsError):
+            hs.hs_resolve_tokens(pool.handle, 0, 1, T, t, pool.step, t.clone())
+        pool.close()
+
+
+def test_four_verify_tokens_scaled_down():
+    """T = 4 verify tokens of K 2048 (8,192 entries per unit), B = 6 K."""
+    w = W.make("spec", R=4, steps=5, tokens=4)
+    replay_tokens(w, attn_steps={0, 4})
+
+
+def test_four_verify_tokens_full_size_decode_step():
+    """32 requests x 2 layers, T = 4, K 2048, B 12288, through hs_decode_step_tokens."""
+    w = W.make("spec", steps=4, tokens=4)
+    replay_step_tokens(w, check_steps={3}, attn_requests={0, 17})
 
 
 def replay_step_tokens(w, check_steps, attn_requests, same_stream=False, kv_format=0):
