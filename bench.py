@@ -6,8 +6,9 @@ sparse layers, ctx 65536, top-K 2048, B 4096, 128 heads; 70% step-to-step
 selection reuse, the rest uniform): for each layer, RESOLVE (page table + LRU
 hot buffer + miss copies from pinned host memory) then sparse MLA decode
 attention over the K resolved rows, then the step counter advances.  The step
-is one hs_decode_step call: layer l+1's RESOLVE runs on a copy stream beside
-layer l's attention ("precise prefetch").  Per-kernel rooflines come from a
+is one hs_decode_step call: the later layers' RESOLVE runs on a copy stream
+("precise prefetch"; bf16 rows: beside layer 0's RESOLVE, FP8 rows: after it,
+beside layer 0's attention).  Per-kernel rooflines come from a
 second timed pass of the same workload with the calls made one after another
 on one stream (CUDA events around each launch).  Inputs (top-K traces,
 queries) are resident in HBM before the timed region.
@@ -417,7 +418,7 @@ def run_ours(args):
         lib.hs_step_advance(step_ptr, sptr)
 
     def fused_step(t, ev=None):
-        """One hs_decode_step call: layer l+1's RESOLVE beside layer l's attention."""
+        """One hs_decode_step call (the later layers' RESOLVE on the copy stream)."""
         st = lib.hs_decode_step(ph, 0, L, tk_base + t * tk_stride_t,
                                 q_base + (t % Q_DISTINCT) * q_stride_t, H, W.V_DIM, W.SCALE,
                                 step_ptr, rows_d.data_ptr(), out_d.data_ptr(), lse_d.data_ptr(),
@@ -560,9 +561,11 @@ def run_ours(args):
             "miss_rows_per_step": misses_main / args.steps,
             "cold_step": {"ms": cold_ms, "miss_rows": cold_misses,
                           "note": "step 0 (empty hot buffers), before the warm-up; not in value"},
-            "schedule": ("hs_decode_step: RESOLVE of layer l+1 on a copy stream beside layer l's "
-                         "attention; per-kernel rooflines from a sequential pass of "
-                         f"{n_ev} steps") if attention else "sequential, one stream",
+            "schedule": ("hs_decode_step: the later layers' RESOLVE on a copy stream "
+                         + ("after layer 0's RESOLVE, beside its attention" if fp8 else
+                            "beside layer 0's RESOLVE")
+                         + f"; per-kernel rooflines from a sequential pass of {n_ev} steps")
+            if attention else "sequential, one stream",
             "roofline": dominant,
             "kernels": [resolve_roof, att_roof],
             "host_link_peak_gbs": h2d_peak,
