@@ -386,6 +386,15 @@ hs_status hs_commit_offload(hs_pool* pool, int32_t req, int32_t page,
  * null or misaligned pointers. */
 hs_status hs_host_read(const void* host_device_ptr, int64_t bytes, void* dst, void* stream);
 
+/* Self-test of the in-kernel bounded waits that keep a stalled hand-off from
+ * hanging the GPU: two one-thread kernels each wait on an mbarrier of their
+ * own CTA that nothing arrives on, with the waits the attention kernel and
+ * RESOLVE use, limited to timeout_ns (1 .. 1e8) instead of their 1 s.
+ * result: device int32[2], set on `stream` to [the error bits the attention
+ * wait raised (WAIT expected), 1 if RESOLVE's wait gave up].  HS_ERR_INVALID
+ * for a null result or a timeout out of range. */
+hs_status hs_selftest_bounded_waits(int64_t timeout_ns, int32_t* result, void* stream);
+
 /* *d_step += 1 on `stream` (graph-capturable). */
 hs_status hs_step_advance(int32_t* d_step, void* stream);
 

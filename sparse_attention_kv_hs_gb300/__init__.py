@@ -44,6 +44,7 @@ EXPORTED = (
     "hs_sparse_mla_decode", "hs_offload_prefix", "hs_offload_pages", "hs_commit_offload",
     "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
     "hs_sparse_mla_decode_noalloc", "hs_decode_step", "hs_decode_step_tokens", "hs_resolve_tokens",
+    "hs_selftest_bounded_waits",
     "hs_sparse_mla_decode_tokens",
 )
 
@@ -104,6 +105,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_sparse_mla_decode": [p, i32, p, p, i32, i32, f32, p, p, p],
         "hs_offload_prefix": [p, i32, i32, p, p, p],
         "hs_offload_pages": [p, i32, p, p, p, p, p],
+        "hs_selftest_bounded_waits": [i64, p, p],
         "hs_commit_offload": [p, i32, i32, p, p],
         "hs_step_advance": [p, p],
         "hs_check_errors": [p, ctypes.POINTER(i32)],
@@ -279,6 +281,12 @@ def hs_decode_step_tokens(pool: int, layer_begin: int, num_layers: int, num_toke
 def hs_offload_prefix(pool: int, req: int, page: int, main_stream, side_stream, done_event) -> None:
     _check(load().hs_offload_prefix(pool, req, page, _stream(main_stream), _stream(side_stream),
                                     _event(done_event)), "hs_offload_prefix")
+
+
+def hs_selftest_bounded_waits(timeout_ns: int, result, stream=None) -> None:
+    """Run the bounded-wait self-test; `result` a device int32[2] tensor."""
+    _check(load().hs_selftest_bounded_waits(int(timeout_ns), _addr(result), _stream(stream)),
+           "hs_selftest_bounded_waits")
 
 
 def hs_offload_pages(pool: int, reqs, pages, main_stream, side_stream, done_event) -> None:

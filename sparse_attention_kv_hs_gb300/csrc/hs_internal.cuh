@@ -82,6 +82,9 @@ hs_status hs_launch_attention_tokens(hs_pool* pool, int32_t layer, int32_t num_t
                                      const void* q, const int32_t* row_ids, int32_t num_heads,
                                      int32_t v_dim, float scale, void* out, float* lse,
                                      int max_splits, cudaStream_t stream);
+// One-thread kernel: RESOLVE's bounded wait on a barrier nothing arrives on.
+hs_status hs_launch_peer_wait_selftest(int32_t* gave_up, uint64_t timeout_ns,
+                                       cudaStream_t stream);
 hs_status hs_attn_workspace_init(hs_pool* pool);
 void hs_attn_workspace_free(hs_pool* pool);
 // Shared memory the RESOLVE kernel needs for these sizes; sets the kernel's

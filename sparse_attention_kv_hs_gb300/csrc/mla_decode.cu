@@ -167,10 +167,12 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-// Bounded wait on a local mbarrier; on timeout (or if the CTA is already
-// aborting) returns false and raises the abort flag.
+// Bounded wait on a local mbarrier; on timeout (timeout_ns of the global
+// timer, or at once if the CTA is already aborting) returns false, raises the
+// abort flag and sets error bit WAIT.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort,
-                                         int32_t* error_word, bool cluster_scope = false) {
+                                         int32_t* error_word, bool cluster_scope = false,
+                                         uint64_t timeout_ns = kWaitNs) {
   if (*abort) return false;
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
@@ -181,7 +183,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       const uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitNs) {
+      } else if (now - t0 > timeout_ns) {
         *abort = 1;
         atomicOr(error_word, HS_DEV_ERR_WAIT);
         return false;
@@ -1121,6 +1123,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // Combine per-split normalised partials: o = sum_c w_c o_c / sum_c w_c with
 // w_c = exp(lse_c - max lse).  One CTA per (request, head), 128 threads x 4.
+// Self-test of wait_bar's time limit: one thread waits on a barrier of its
+// CTA that nothing arrives on, and gives up after timeout_ns.
+__global__ void wait_selftest_kernel(int32_t* error_word, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bar(smem_u32(&bar), 0, &abort_flag, error_word, false, timeout_ns);
+}
+
 __global__ void __launch_bounds__(128) merge_splits_kernel(const float* __restrict__ ws_o,
                                                            const float* __restrict__ ws_lse,
                                                            int splits, int H,
@@ -1427,4 +1442,13 @@ extern "C" hs_status hs_sparse_mla_decode_noalloc(const void* kv_rows, int64_t n
   a.splits = splits;
   a.scale_log2 = scale * 1.4426950408889634f;
   return launch_decode(a, kv_map, q, num_requests, hs_stream(stream));
+}
+
+extern "C" hs_status hs_selftest_bounded_waits(int64_t timeout_ns, int32_t* result, void* stream) {
+  if (!result || timeout_ns <= 0 || timeout_ns > 100000000) return HS_ERR_INVALID;
+  cudaStream_t st = hs_stream(stream);
+  HS_CUDA_TRY(cudaMemsetAsync(result, 0, 2 * sizeof(int32_t), st));
+  wait_selftest_kernel<<<1, 32, 0, st>>>(result, (uint64_t)timeout_ns);
+  HS_CUDA_TRY(cudaGetLastError());
+  return hs_launch_peer_wait_selftest(result + 1, (uint64_t)timeout_ns, st);
 }

@@ -128,8 +128,9 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 
 // Bounded wait (acquire, cluster scope) for phase `parity` of a local mbarrier
-// that peers arrive on remotely; false after kWaitNs.
-__device__ __forceinline__ bool wait_peer_bar(uint32_t bar, uint32_t parity) {
+// that peers arrive on remotely; false after timeout_ns of the global timer.
+__device__ __forceinline__ bool wait_peer_bar(uint32_t bar, uint32_t parity,
+                                              uint64_t timeout_ns = kWaitNs) {
   uint64_t t0 = 0;
   for (uint32_t i = 0;; ++i) {
     if (hs_ptx::mbar_try_wait_cluster(bar, parity)) return true;
@@ -137,7 +138,7 @@ __device__ __forceinline__ bool wait_peer_bar(uint32_t bar, uint32_t parity) {
       const uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitNs) {
+      } else if (now - t0 > timeout_ns) {
         return false;
       }
     }
@@ -148,8 +149,6 @@ __device__ __forceinline__ uint32_t hash_pos(int32_t p, int bits) {
   return ((uint32_t)p * 0x9E3779B1u) >> (32 - bits);
 }
 
-// Selection hash in shared memory (open addressing, linear probing; key -1 =
-// empty): position -> the smallest list index j that selects it.
 // Selection hash over a list (open addressing, linear probing): a slot holds
 // the first index j of the list whose entry is the slot's position, or -1;
 // the position itself is read back from the list.  Inserts may run
@@ -634,6 +633,15 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   copy_host_rows(hsrc, kdst, rv, n_early, n_serve, [&](int i) { return s_miss_p[i]; }, slot_row);
 }
 
+// Self-test of wait_peer_bar's time limit: one thread waits on a barrier of
+// its CTA that nothing arrives on; *gave_up = 1 once the wait returns false.
+__global__ void peer_wait_selftest_kernel(int32_t* gave_up, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) hs_ptx::mbar_init(hs_ptx::smem_u32(&bar), 1);
+  __syncthreads();
+  if (threadIdx.x == 0) *gave_up = wait_peer_bar(hs_ptx::smem_u32(&bar), 0, timeout_ns) ? 0 : 1;
+}
+
 int ceil_log2(int64_t x) {
   int b = 0;
   while ((int64_t(1) << b) < x) ++b;
@@ -777,6 +785,13 @@ hs_status hs_launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers,
                             cudaStream_t stream) {
   return launch_resolve(p, layer_begin, num_layers, 1, topk, d_step, out_rows, miss_count,
                         miss_log, max_cluster, stream);
+}
+
+hs_status hs_launch_peer_wait_selftest(int32_t* gave_up, uint64_t timeout_ns,
+                                       cudaStream_t stream) {
+  peer_wait_selftest_kernel<<<1, 32, 0, stream>>>(gave_up, timeout_ns);
+  HS_CUDA_TRY(cudaGetLastError());
+  return HS_OK;
 }
 
 hs_status hs_launch_resolve_tokens(hs_pool* p, int32_t layer_begin, int32_t num_layers,
