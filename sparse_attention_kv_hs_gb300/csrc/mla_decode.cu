@@ -27,7 +27,11 @@
 // TMA (tile::gather4, 128-byte swizzle, straight into the operand layout);
 // CTA 1's eight loader warps move the 512 value columns with 16-byte vector
 // loads, converting them to fp16 through registers, with the loads for the
-// next tile issued before the stage frees up.  Q reaches CTA 0 by TMA
+// next tile issued before the stage frees up.  Pools of FP8 rows (656 bytes:
+// E4M3 latent codes with one scale per 128 values, bf16 rope) are read by
+// vector loads in both CTAs and dequantized to fp16 operands on the way into
+// shared memory (Fp8Loader); the score MMA then runs on fp16, with Q
+// converted from bf16 as it moves to tensor memory.  Q reaches CTA 0 by TMA
 // (swizzled, then TMEM), each split's row ids are staged in shared memory
 // once, MMA descriptors are computed once and advanced by constants, and
 // every hand-off is an mbarrier.  With several splits per request, each pair
