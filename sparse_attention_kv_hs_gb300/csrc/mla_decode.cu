@@ -916,25 +916,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!wait_bar_warp(bar(B_S_FULL + b), pb, abort_flag, a.error_word)) break;
       tc_fence_after();
       const uint32_t sa = tm + lane_off + TM_S + b * kTile;
-      // Two passes over S in tensor memory, 32 columns at a time (few live
-      // registers): the tile max of the raw scores first (scale > 0 keeps the
-      // order; rows without a valid id do not count), then the exponents.
+      // One read of the tile's 64 scores from tensor memory: the tile max of
+      // the raw scores (scale > 0 keeps the order; rows without a valid id do
+      // not count), then the exponents from the same registers.
+      uint32_t u[64];
+      tmem_ld16p(sa, u);
+      tmem_ld16p(sa + 16, u + 16);
+      tmem_ld16p(sa + 32, u + 32);
+      tmem_ld16p(sa + 48, u + 48);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_S_EMPTY + b));  // S buffer b read out
       float tmax = -INFINITY;
+      if (valid == ~0ull) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t u[32];
-        tmem_ld16p(sa + 32 * half, u);
-        tmem_ld16p(sa + 32 * half + 16, u + 16);
-        tmem_ld_wait();
-        const uint32_t vbits = (uint32_t)(valid >> (32 * half));
-        if (vbits == ~0u) {
+        for (int i = 0; i < 64; ++i) tmax = fmaxf(tmax, __uint_as_float(u[i]));
+      } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, __uint_as_float(u[i]));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if ((vbits >> i) & 1) tmax = fmaxf(tmax, __uint_as_float(u[i]));
-        }
+        for (int i = 0; i < 64; ++i)
+          if ((valid >> i) & 1) tmax = fmaxf(tmax, __uint_as_float(u[i]));
       }
       tmax *= a.scale_log2;
       // lazy rescale: move the reference max only when it grew by > 2^8
@@ -951,35 +951,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // p = 2^(scale_log2 * x - m_used); invalid rows give p = 0.  m_used is -inf
       // only while no valid row has been seen, and then every p is 0.
       const float neg_m = -m_used;
-      const bool none_yet = m_used == -INFINITY;
+      const uint64_t vb = m_used == -INFINITY ? 0ull : valid;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t u[32];
-        tmem_ld16p(sa + 32 * half, u);
-        tmem_ld16p(sa + 32 * half + 16, u + 16);
-        tmem_ld_wait();
-        const uint32_t vbits = none_yet ? 0u : (uint32_t)(valid >> (32 * half));
+      for (int kbg = 0; kbg < 8; ++kbg) {
+        uint32_t pk[4];
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = kb * 8 + 2 * i;
-            float p0 = fast_exp2(fmaf(__uint_as_float(u[j]), a.scale_log2, neg_m));
-            float p1 = fast_exp2(fmaf(__uint_as_float(u[j + 1]), a.scale_log2, neg_m));
-            p0 = ((vbits >> j) & 1) ? p0 : 0.f;
-            p1 = ((vbits >> (j + 1)) & 1) ? p1 : 0.f;
-            l_sum += p0 + p1;
-            pk[i] = pack_f16x2(p0, p1);
-          }
-          // P [128 heads x 64 rows], K-major core matrices (head group, row group)
-          const int kbg = half * 4 + kb;
-          const uint32_t off = (uint32_t)(((h >> 3) * (kTile / 8) + kbg) * 128 + (h & 7) * 16);
-          *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        for (int i = 0; i < 4; ++i) {
+          const int j = kbg * 8 + 2 * i;
+          float p0 = fast_exp2(fmaf(__uint_as_float(u[j]), a.scale_log2, neg_m));
+          float p1 = fast_exp2(fmaf(__uint_as_float(u[j + 1]), a.scale_log2, neg_m));
+          p0 = ((vb >> j) & 1) ? p0 : 0.f;
+          p1 = ((vb >> (j + 1)) & 1) ? p1 : 0.f;
+          l_sum += p0 + p1;
+          pk[i] = pack_f16x2(p0, p1);
         }
+        // P [128 heads x 64 rows], K-major core matrices (head group, row group)
+        const uint32_t off = (uint32_t)(((h >> 3) * (kTile / 8) + kbg) * 128 + (h & 7) * 16);
+        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      tc_fence_before();
-      mbar_arrive(bar(B_S_EMPTY + b));  // S buffer b read out
       reinterpret_cast<float*>(pbuf + kPAlphaOff)[h] = alpha;
       const uint32_t any = __ballot_sync(0xffffffffu, rescale && t > 0);
       if (lane == 0) reinterpret_cast<uint32_t*>(pbuf + kPFlagOff + 16 * wq)[0] = any;
