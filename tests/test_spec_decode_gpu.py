@@ -228,3 +228,41 @@ def test_decode_step_tokens_on_one_stream_scaled_down():
 def test_decode_step_tokens_fp8_rows():
     w = W.make("spec", R=4, steps=4)
     replay_step_tokens(w, check_steps={0, 3}, attn_requests=set(range(4)), kv_format=1)
+
+
+def test_decode_step_tokens_graph_captured():
+    """One speculative step (two streams, events, step counter) captured once
+    and replayed: row ids and miss counts match the oracle every step."""
+    w = W.make("spec", R=3, steps=4)
+    scen = W.Scenario.build(w)
+    pool = harness.make_pool(w, scen)
+    o = harness.make_oracle(w, scen)
+    R, L, K, T, H = w.R, w.L, w.K, w.tokens, w.heads
+    tr = np.stack([w.trace_tokens(r) for r in range(R)], axis=2)  # [steps][L][R][T][K]
+    d_topk = torch.empty((L, R, T, K), dtype=torch.int32, device="cuda")
+    d_rows = torch.empty((L, R, T, K), dtype=torch.int32, device="cuda")
+    d_cnt = torch.empty((L, R), dtype=torch.int32, device="cuda")
+    d_q = torch.zeros((L, R, T, H, W.ROW_ELEMS), dtype=torch.int16, device="cuda")
+    d_o = torch.empty((L, R, T, H, W.V_DIM), dtype=torch.bfloat16, device="cuda")
+    main, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(main):
+        with torch.cuda.graph(g, stream=main):
+            hs.hs_decode_step_tokens(pool.handle, 0, L, T, d_topk, d_q, H, W.V_DIM, W.SCALE,
+                                     pool.step, d_rows, d_o, None, d_cnt, main, copy)
+            hs.hs_step_advance(pool.step, main)
+    for t in range(w.steps):
+        d_topk.copy_(torch.from_numpy(tr[t]))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        rows, cnt = d_rows.cpu().numpy(), d_cnt.cpu().numpy()
+        for l in range(L):
+            for r in range(R):
+                ref_rows, ref_log, err = o.resolve_tokens(l, r, tr[t, l, r], t)
+                assert err == 0
+                np.testing.assert_array_equal(rows[l, r], ref_rows, err_msg=f"t={t} l={l} r={r}")
+                assert cnt[l, r] == len(ref_log)
+    assert hs.hs_check_errors(pool.handle) == 0
+    pool.close()
