@@ -231,10 +231,10 @@ hs_status hs_gather(hs_pool* pool, int32_t layer, const int32_t* row_ids,
  * (that request's output is then not meaningful).
  * FP8 pools (HS_KV_FP8): both products run on fp16 operands.  q is rounded
  * from bf16 to fp16; a latent value is E4M3(code) * scale formed as fp16 --
- * from the scale rounded to fp16 when the row group's scale is 0 or in
- * [2^-14, 146] (so no code can overflow), else in fp32 and rounded once --
- * and a rope value is converted from bf16.  An operand fp16 cannot hold, or
- * a NaN code, sets VALUE.
+ * from the scale rounded to fp16 when every group scale of the 8 rows a
+ * loader warp handles in that tile is 0 or in [2^-14, 146] (so no code can
+ * overflow), else in fp32 and rounded once -- and a rope value is converted
+ * from bf16.  An operand fp16 cannot hold, or a NaN code, sets VALUE.
  *   q        device bf16 [R][num_heads][row_elems]   (num_heads <= 128)
  *   row_ids  device int32 [R][K] (e.g. hs_resolve's output for this layer)
  *   out      device bf16 [R][num_heads][v_dim]
