@@ -1135,21 +1135,43 @@ __global__ void __launch_bounds__(128) merge_splits_kernel(const float* __restri
                                                            uint16_t* __restrict__ out,
                                                            float* __restrict__ lse_out) {
   const int r = blockIdx.y, h = blockIdx.x;
-  float mx = -INFINITY;
-  for (int c = 0; c < splits; ++c) mx = fmaxf(mx, ws_lse[((int64_t)r * splits + c) * kHeads + h]);
-  float wsum = 0.f;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   const int e0 = threadIdx.x * 4;
-  for (int c = 0; c < splits; ++c) {
-    const float lc = ws_lse[((int64_t)r * splits + c) * kHeads + h];
-    const float w = lc == -INFINITY ? 0.f : expf(lc - mx);
-    wsum += w;
-    const float4 o = *reinterpret_cast<const float4*>(
-        ws_o + (((int64_t)r * splits + c) * kHeads + h) * kDV + e0);
-    acc[0] += w * o.x;
-    acc[1] += w * o.y;
-    acc[2] += w * o.z;
-    acc[3] += w * o.w;
+  const float* lse_rh = ws_lse + (int64_t)r * splits * kHeads + h;
+  const float* o_rh = ws_o + ((int64_t)r * splits * kHeads + h) * kDV + e0;
+  // Splits in groups of four, each group's loads issued together: a running
+  // max with the sums rescaled when it grows (with at most four splits, one
+  // group: the plain max-then-weights sum).
+  float mx = -INFINITY, wsum = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c0 = 0; c0 < splits; c0 += 4) {
+    float lc[4];
+    float4 o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int c = c0 + u;
+      lc[u] = c < splits ? lse_rh[(int64_t)c * kHeads] : -INFINITY;
+      o[u] = c < splits ? *reinterpret_cast<const float4*>(o_rh + (int64_t)c * kHeads * kDV)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m_new = mx;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m_new = fmaxf(m_new, lc[u]);
+    if (mx != -INFINITY && m_new > mx) {  // rescale what earlier groups summed
+      const float k = expf(mx - m_new);
+      wsum *= k;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] *= k;
+    }
+    mx = m_new;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = lc[u] == -INFINITY ? 0.f : expf(lc[u] - mx);
+      wsum += w;
+      acc[0] += w * o[u].x;
+      acc[1] += w * o[u].y;
+      acc[2] += w * o[u].z;
+      acc[3] += w * o[u].w;
+    }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   uint2 pk;
