@@ -22,12 +22,13 @@
  * are copied to host in one launch covering all sparse layers.
  *
  * Data layout (all owned by the pool unless stated):
- *   KV row        row_elems bf16 values (576 = 512 latent + 64 rope)
- *   kv_pool       device  bf16 [L][blocks_per_layer][P][row_elems]
+ *   KV row        row_elems bf16 values (576 = 512 latent + 64 rope), or a
+ *                 656-byte FP8 row (kv_format HS_KV_FP8, below)
+ *   kv_pool       device [L][blocks_per_layer][P] rows
  *                 blocks 0 .. R*B/P-1 of every layer are the hot buffers:
  *                 request r's hot slot s is block r*(B/P) + s/P, row s%P;
  *                 blocks from R*B/P on hold resident pages
- *   host_pool     pinned, mapped host bf16 [L][host_tokens][row_elems];
+ *   host_pool     pinned, mapped host [L][host_tokens] rows;
  *                 request r's position p of layer l is row host_off[r] + p
  *   row id        index of a row within one layer of kv_pool:
  *                 block * P + offset (-1 = no row)
@@ -208,10 +209,11 @@ hs_status hs_resolve_tokens(hs_pool* pool, int32_t layer_begin, int32_t num_laye
                             int32_t* miss_count, int32_t* miss_log, void* stream);
 
 /* Gather rows of one layer by row id ("one stride"): out_rows[i] =
- * kv_pool[layer][row_ids[i]] (row_elems bf16 each); row id -1 gives a zero
- * row.  row_ids: device int32 [n_rows]; out_rows: device bf16
- * [n_rows][row_elems] (caller-owned).  Async, graph-capturable.  A row id
- * outside the layer writes a zero row and sets error bit BLOCK. */
+ * kv_pool[layer][row_ids[i]] (one row of the pool's format: row_elems bf16,
+ * or 656 bytes for HS_KV_FP8); row id -1 gives a zero row.  row_ids: device
+ * int32 [n_rows]; out_rows: device [n_rows][row bytes] (caller-owned).
+ * Async, graph-capturable.  A row id outside the layer writes a zero row and
+ * sets error bit BLOCK. */
 hs_status hs_gather(hs_pool* pool, int32_t layer, const int32_t* row_ids,
                     int64_t n_rows, void* out_rows, void* stream);
 
