@@ -517,8 +517,10 @@ struct Fp8Loader {
           for (int q = 0; q < 4; ++q) {
             o[2 * q] = mul_f16x2(e4m3x2_to_f16x2(w[q] & 0xffffu), s2);
             o[2 * q + 1] = mul_f16x2(e4m3x2_to_f16x2(w[q] >> 16), s2);
-            nan0 = max_nan_f16x2(nan0, o[2 * q]);
-            nan1 = max_nan_f16x2(nan1, o[2 * q + 1]);
+            if (!ROPE) {  // the score CTA forms the same values: one check suffices
+              nan0 = max_nan_f16x2(nan0, o[2 * q]);
+              nan1 = max_nan_f16x2(nan1, o[2 * q + 1]);
+            }
           }
           half[0] = make_uint4(o[0], o[1], o[2], o[3]);
           half[1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -551,7 +553,7 @@ struct Fp8Loader {
         st_shared_v4(base + 8u * kBlockBytes + (((uint32_t)k ^ ph) << 4), x);
       }
     }
-    if (FAST) {
+    if (FAST && !ROPE) {
       const uint32_t n = max_nan_f16x2(nan0, nan1);
       if ((n & 0x7fffu) > 0x7c00u || (n & 0x7fff0000u) > 0x7c000000u) vmax |= 0x7C00u;
     }
