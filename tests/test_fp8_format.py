@@ -66,3 +66,27 @@ def test_rows_at_matches_contiguous_fill():
         np.testing.assert_array_equal(got[i], want)
     big = synth.rows_fp8(1006, 2, 0, 0, 5000, threads=4)
     np.testing.assert_array_equal(big[300], got[3])
+
+
+def test_e4m3_codes_worked_by_hand():
+    """Codes decoded from E4M3's definition (sign, 4 exponent bits with bias 7,
+    3 mantissa bits; exponent 0 is subnormal, 0x7F/0xFF are NaN), by hand."""
+    cases = {
+        0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+        0x30: 0.5, 0x38: 1.0, 0x3C: 1.5, 0x40: 2.0, 0x77: 240.0, 0x7E: 448.0,
+        0x80: -0.0, 0xB8: -1.0, 0xFE: -448.0,
+    }
+    for code, value in cases.items():
+        assert oracle.E4M3_TABLE[code] == value, hex(code)
+    assert np.isnan(oracle.E4M3_TABLE[0x7F]) and np.isnan(oracle.E4M3_TABLE[0xFF])
+    assert np.signbit(oracle.E4M3_TABLE[0x80])
+    # one row by hand: codes 0x38 (1.0) and 0x3C (1.5), group scales 0.5 .. 2
+    raw = np.zeros((1, 656), dtype=np.uint8)
+    raw[0, :512] = np.where(np.arange(512) % 2 == 0, 0x38, 0x3C)
+    raw[0, 512:528] = np.array([0.5, 1.0, 1.5, 2.0], dtype=np.float32).view(np.uint8)
+    raw[0, 528:656] = np.full(64, 0x3F80, dtype=np.uint16).view(np.uint8)    # bf16 1.0
+    row = oracle.fp8_rows_to_f64(raw)[0]
+    for g, sc in enumerate((0.5, 1.0, 1.5, 2.0)):
+        np.testing.assert_array_equal(row[128 * g:128 * g + 128:2], sc * 1.0)
+        np.testing.assert_array_equal(row[128 * g + 1:128 * g + 128:2], sc * 1.5)
+    np.testing.assert_array_equal(row[512:], 1.0)
