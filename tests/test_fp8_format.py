@@ -90,3 +90,15 @@ def test_e4m3_codes_worked_by_hand():
         np.testing.assert_array_equal(row[128 * g:128 * g + 128:2], sc * 1.0)
         np.testing.assert_array_equal(row[128 * g + 1:128 * g + 128:2], sc * 1.5)
     np.testing.assert_array_equal(row[512:], 1.0)
+
+
+def test_e4m3_encoding_worked_by_hand():
+    """The generator's encoder on values worked by hand: exact codes, a tie
+    rounded to the even mantissa, saturation, and the subnormal range."""
+    cases = [(1.0, 0x38), (-0.75, 0xB4), (448.0, 0x7E), (1000.0, 0x7E), (-1000.0, 0xFE),
+             (1.0625, 0x38),          # halfway between 1.0 (mantissa 000) and 1.125: even
+             (1.1875, 0x3A),          # halfway between 1.125 and 1.25 (mantissa 010): even
+             (2.0 ** -9, 0x01), (3 * 2.0 ** -10, 0x02),   # 1.5 x 2^-9: tie to even (2 x 2^-9)
+             (0.0, 0x00)]
+    for value, code in cases:
+        assert synth.e4m3_encode(value) == code, (value, hex(synth.e4m3_encode(value)))
