@@ -333,8 +333,14 @@ hs_status hs_sparse_mla_decode_tokens(hs_pool* pool, int32_t layer, int32_t num_
  *   kv_rows   device bf16 [num_rows][576]: the layer's KV rows, row ids index it
  *   q         device bf16 [num_requests][num_heads][576]
  *   row_ids   device int32 [num_requests][top_k] (-1 = padding; an id outside
- *             [0, num_rows) is excluded like padding and is not reported)
+ *             [0, num_rows) is excluded like padding and sets error bit BLOCK)
  *   out, lse  as for hs_sparse_mla_decode
+ * Device-side errors go to an error word of the library's own (one per
+ * device, shared by every call), which hs_noalloc_check_errors reads and
+ * clears: BLOCK as above, VALUE (as for hs_sparse_mla_decode: the output of
+ * that call is not meaningful), WAIT (a bounded wait gave up; the output is
+ * not meaningful) and INTERNAL (the kernel found its launch set-up unusable
+ * and did nothing).
  * It calls no cudaMalloc, cudaFree or other allocating routine: its split-K
  * scratch is a fixed device array of this library (16 MiB + 32 KiB, held by
  * every GPU that loads the library until the process exits), big enough for
@@ -349,6 +355,15 @@ hs_status hs_sparse_mla_decode_noalloc(const void* kv_rows, int64_t num_rows, co
                                        const int32_t* row_ids, int32_t num_requests,
                                        int32_t top_k, int32_t num_heads, int32_t v_dim,
                                        float scale, void* out, float* lse, void* stream);
+
+/* Synchronise the current device, then read and clear the error word that
+ * hs_sparse_mla_decode_noalloc calls on this device OR their device-side
+ * error bits into (BLOCK, VALUE, WAIT, INTERNAL; see there).  Allocates
+ * nothing (a 4-byte copy each way between host and the library's fixed
+ * device word).  No counterpart on the pages: it is the error channel of the
+ * allocation-free call.  Returns HS_OK if the word was zero, HS_ERR_DEVICE
+ * otherwise; *code_out (if not NULL) receives the bits. */
+hs_status hs_noalloc_check_errors(int32_t* code_out);
 
 /* Prefix offload: copy page `page` of request `req` (all layers, from the
  * block the page table maps it to) into its rows of the host pool.  The copy

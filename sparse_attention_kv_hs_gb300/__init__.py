@@ -45,7 +45,7 @@ EXPORTED = (
     "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
     "hs_sparse_mla_decode_noalloc", "hs_decode_step", "hs_decode_step_tokens", "hs_resolve_tokens",
     "hs_selftest_bounded_waits",
-    "hs_sparse_mla_decode_tokens",
+    "hs_sparse_mla_decode_tokens", "hs_noalloc_check_errors",
 )
 
 
@@ -115,6 +115,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_decode_step_tokens": [p, i32, i32, i32, p, p, i32, i32, f32, p, p, p, p, p, p, p],
         "hs_resolve_tokens": [p, i32, i32, i32, p, p, p, p, p, p],
         "hs_sparse_mla_decode_tokens": [p, i32, i32, p, p, i32, i32, f32, p, p, p],
+        "hs_noalloc_check_errors": [ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -254,6 +255,16 @@ def hs_sparse_mla_decode_noalloc(kv_rows, num_rows: int, q, row_ids, num_request
                                                num_requests, top_k, num_heads, v_dim, scale,
                                                _addr(out), _addr(lse), _stream(stream)),
            "hs_sparse_mla_decode_noalloc")
+
+
+def hs_noalloc_check_errors() -> int:
+    """Synchronise, read and clear the allocation-free call's device error
+    word on the current device; returns its bits."""
+    code = ctypes.c_int32(0)
+    st = load().hs_noalloc_check_errors(ctypes.byref(code))
+    if st not in (HS_OK, HS_ERR_DEVICE):
+        raise HsError(st, "hs_noalloc_check_errors")
+    return code.value
 
 
 def hs_decode_step(pool: int, layer_begin: int, num_layers: int, topk_idx, q, num_heads: int,

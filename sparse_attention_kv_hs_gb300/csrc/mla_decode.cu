@@ -1461,6 +1461,21 @@ extern "C" hs_status hs_sparse_mla_decode_noalloc(const void* kv_rows, int64_t n
   return launch_decode(a, kv_map, q, num_requests, hs_stream(stream));
 }
 
+extern "C" hs_status hs_noalloc_check_errors(int32_t* code_out) {
+  int dev = 0;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return HS_ERR_INVALID;
+  const hs_status st = noalloc_setup(dev);
+  if (st != HS_OK) return st;
+  HS_CUDA_TRY(cudaDeviceSynchronize());
+  int32_t code = 0;
+  HS_CUDA_TRY(cudaMemcpy(&code, g_noalloc_err_ptr[dev], sizeof(code), cudaMemcpyDeviceToHost));
+  const int32_t zero = 0;
+  HS_CUDA_TRY(cudaMemcpy(g_noalloc_err_ptr[dev], &zero, sizeof(zero), cudaMemcpyHostToDevice));
+  if (code_out) *code_out = code;
+  return code ? HS_ERR_DEVICE : HS_OK;
+}
+
 extern "C" hs_status hs_selftest_bounded_waits(int64_t timeout_ns, int32_t* result, void* stream) {
   if (!result || timeout_ns <= 0 || timeout_ns > 100000000) return HS_ERR_INVALID;
   cudaStream_t st = hs_stream(stream);

@@ -1,7 +1,8 @@
 // Thin inline-PTX wrappers for the Blackwell (sm_100 family, here sm_103a)
 // features the attention kernel uses: mbarriers (with bounded waits),
 // tensor memory (tcgen05.alloc / ld / st), tcgen05.mma with fp32
-// accumulation in TMEM, cp.async row staging, and cluster shared memory.
+// accumulation in TMEM, shared-memory matrix descriptors, and cluster
+// shared memory (remote arrivals, bulk copies between the CTAs of a cluster).
 #pragma once
 
 #include <cuda_runtime.h>
