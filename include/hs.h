@@ -124,8 +124,20 @@ typedef struct hs_pool hs_pool; /* opaque, library-owned */
  * leased once per (request, layer), then resident blocks), the page table
  * (all host-only), LRU metadata (all slots empty, stamp -1), the step counter
  * (0) and the attention workspace.  Synchronous.  On failure *out is NULL and
- * nothing stays allocated.  Host-pool contents are left uninitialised. */
+ * nothing stays allocated: HS_ERR_OOM when an allocation fails, and before any
+ * allocation (and any CUDA call) when the host pool is larger than the
+ * machine's physical memory.  Host-pool contents are left uninitialised. */
 hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out);
+
+/* The host NUMA node the pool's pinned host pool was placed on, or -1.
+ * hs_pool_create places it on the node CUDA reports as nearest the device
+ * (preferred-node policy, then registered pinned and mapped), so that on a
+ * machine with several sockets each replica's miss reads stay local (page
+ * "GLM 5.3 Optimizations, Part 1", section "Composition with the rest of
+ * vLLM": one pinned host pool per data-parallel replica); -1 when the device
+ * reports no host node or the placement was refused (then cudaHostAlloc
+ * placed it). */
+hs_status hs_pool_host_numa_node(const hs_pool* pool, int32_t* node_out);
 
 /* Free everything the pool owns.  Synchronises the device first. */
 hs_status hs_pool_destroy(hs_pool* pool);
@@ -395,6 +407,18 @@ hs_status hs_offload_pages(hs_pool* pool, int32_t num_pages, const int32_t* reqs
  * (page_table = -1).  The freed block may be mapped again afterwards. */
 hs_status hs_commit_offload(hs_pool* pool, int32_t req, int32_t page,
                             void* main_stream, void* done_event);
+
+/* Bounded wait, on the host, for an offload to finish: page "GLM 5.3
+ * Optimizations, Part 1", section "How it works" -- the CPU copy of a
+ * completed prefix page serves prefix reuse only once its transfer has
+ * completed.  Polls `done_event` (the event hs_offload_prefix or
+ * hs_offload_pages recorded) every ~20 us without synchronising any stream,
+ * for at most timeout_ns of wall-clock time (0 = one poll).  Returns HS_OK once
+ * the copy has completed (its host rows are then readable), HS_ERR_TIMEOUT if
+ * it has not by then (nothing is cancelled; wait again or commit later),
+ * HS_ERR_CUDA if the event reports an error, HS_ERR_INVALID for a NULL event or
+ * a negative timeout.  An event never recorded counts as complete. */
+hs_status hs_wait_offload(void* done_event, int64_t timeout_ns);
 
 /* Copy `bytes` (a multiple of 16) from mapped pinned host memory (its device
  * alias, e.g. views.host_pool_device) to device memory `dst` with SM loads --

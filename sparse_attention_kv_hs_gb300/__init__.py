@@ -45,7 +45,8 @@ EXPORTED = (
     "hs_step_advance", "hs_check_errors", "hs_status_string", "hs_version", "hs_host_read",
     "hs_sparse_mla_decode_noalloc", "hs_decode_step", "hs_decode_step_tokens", "hs_resolve_tokens",
     "hs_selftest_bounded_waits",
-    "hs_sparse_mla_decode_tokens", "hs_noalloc_check_errors",
+    "hs_sparse_mla_decode_tokens", "hs_noalloc_check_errors", "hs_wait_offload",
+    "hs_pool_host_numa_node",
 )
 
 
@@ -116,6 +117,8 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_resolve_tokens": [p, i32, i32, i32, p, p, p, p, p, p],
         "hs_sparse_mla_decode_tokens": [p, i32, i32, p, p, i32, i32, f32, p, p, p],
         "hs_noalloc_check_errors": [ctypes.POINTER(i32)],
+        "hs_wait_offload": [p, i64],
+        "hs_pool_host_numa_node": [p, ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -315,6 +318,22 @@ def hs_offload_pages(pool: int, reqs, pages, main_stream, side_stream, done_even
 def hs_commit_offload(pool: int, req: int, page: int, main_stream, done_event) -> None:
     _check(load().hs_commit_offload(pool, req, page, _stream(main_stream), _event(done_event)),
            "hs_commit_offload")
+
+
+def hs_wait_offload(done_event, timeout_ns: int) -> int:
+    """Bounded host-side wait for an offload's copy event: HS_OK once it has
+    completed, HS_ERR_TIMEOUT if not within timeout_ns (other statuses raise)."""
+    st = load().hs_wait_offload(_event(done_event), int(timeout_ns))
+    if st not in (HS_OK, HS_ERR_TIMEOUT):
+        raise HsError(st, "hs_wait_offload")
+    return st
+
+
+def hs_pool_host_numa_node(pool: int) -> int:
+    """Host NUMA node the pool's pinned host pool was placed on (-1: not placed)."""
+    node = ctypes.c_int32(-1)
+    _check(load().hs_pool_host_numa_node(pool, ctypes.byref(node)), "hs_pool_host_numa_node")
+    return node.value
 
 
 def hs_step_advance(d_step, stream=None) -> None:

@@ -18,6 +18,8 @@ struct hs_pool {
   void* host_pool;      // pinned host
   void* host_pool_dev;  // device alias
   size_t host_bytes;
+  size_t host_map_len;  // > 0: host_pool is an mmap'd, NUMA-placed, registered region
+  int host_numa_node;   // NUMA node the host pool was placed on, or -1
 
   int32_t* page_table;  // [R][max_pages]
   int32_t* ctx_len;     // [R]

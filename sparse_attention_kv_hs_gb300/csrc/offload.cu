@@ -11,6 +11,9 @@
 // pinned host pool.  The side stream first waits for the main stream (an event
 // the pool owns), then `done` is recorded after the copy; committing a page
 // waits on `done` before marking it host only.
+#include <chrono>
+#include <thread>
+
 #include "hs_internal.cuh"
 
 namespace {
@@ -137,4 +140,22 @@ extern "C" hs_status hs_host_read(const void* host_device_ptr, int64_t bytes, vo
       static_cast<const uint4*>(host_device_ptr), bytes / 16, static_cast<uint4*>(dst));
   HS_CUDA_TRY(cudaGetLastError());
   return HS_OK;
+}
+
+// Bounded host-side wait for an offload's copy event: polls the event (no
+// device-side wait, no stream synchronisation) until it completes or
+// timeout_ns of wall-clock time have passed.
+extern "C" hs_status hs_wait_offload(void* done_event, int64_t timeout_ns) {
+  if (!done_event || timeout_ns < 0) return HS_ERR_INVALID;
+  cudaEvent_t ev = reinterpret_cast<cudaEvent_t>(done_event);
+  const auto t0 = std::chrono::steady_clock::now();
+  const auto limit = std::chrono::nanoseconds(timeout_ns);
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return HS_OK;
+    if (e != cudaErrorNotReady) return HS_ERR_CUDA;
+    cudaGetLastError();  // "not ready" is a state, not an error: leave no trace of it
+    if (std::chrono::steady_clock::now() - t0 >= limit) return HS_ERR_TIMEOUT;
+    std::this_thread::sleep_for(std::chrono::microseconds(20));
+  }
 }

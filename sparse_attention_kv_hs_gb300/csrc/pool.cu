@@ -6,6 +6,10 @@
 // resident pages, all in one per-layer KV tensor (page "GLM 5.3
 // Optimizations, Part 1: Hybrid HiSparse Offloading in vLLM", section "How it
 // works": hot pages are ordinary blocks of the same KV tensor).
+#include <sys/mman.h>
+#include <sys/syscall.h>
+#include <unistd.h>
+
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -73,7 +77,12 @@ __global__ void step_advance_kernel(int32_t* step) { *step += 1; }
 void free_pool(hs_pool* p) {
   if (!p) return;
   cudaFree(p->kv_pool);
-  if (p->host_pool) cudaFreeHost(p->host_pool);
+  if (p->host_pool && p->host_map_len) {
+    cudaHostUnregister(p->host_pool);
+    munmap(p->host_pool, p->host_map_len);
+  } else if (p->host_pool) {
+    cudaFreeHost(p->host_pool);
+  }
   cudaFree(p->page_table);
   cudaFree(p->ctx_len);
   cudaFree(p->host_off);
@@ -93,6 +102,51 @@ void free_pool(hs_pool* p) {
   }
   delete[] p->host_off_mirror;
   delete p;
+}
+
+// The pinned, mapped host pool, placed on the host NUMA node nearest the
+// device when the system reports one: anonymous memory with that node as the
+// preferred policy (the kernel falls back to other nodes only when it is
+// full), then registered with CUDA (pinned and mapped), so a miss's host read
+// crosses no socket boundary on machines with several.  Where the device has
+// no host NUMA node or the policy call is refused, cudaHostAlloc places it.
+hs_status alloc_host_pool(hs_pool* p) {
+  p->host_pool = nullptr;
+  p->host_map_len = 0;
+  p->host_numa_node = -1;
+  int node = -1;
+  if (cudaDeviceGetAttribute(&node, cudaDevAttrHostNumaId, p->device) != cudaSuccess) {
+    cudaGetLastError();
+    node = -1;
+  }
+  const long page = sysconf(_SC_PAGESIZE);
+  if (node >= 0 && node < 1024 && page > 0) {
+    const size_t len = (p->host_bytes + (size_t)page - 1) / (size_t)page * (size_t)page;
+    void* m = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (m != MAP_FAILED) {
+      unsigned long mask[1024 / (8 * sizeof(unsigned long))] = {0};
+      mask[node / (8 * sizeof(unsigned long))] |= 1ul << (node % (8 * sizeof(unsigned long)));
+      const long kPreferred = 1;  // MPOL_PREFERRED
+      if (syscall(SYS_mbind, m, len, kPreferred, mask, (unsigned long)1024 + 1, 0u) == 0 &&
+          cudaHostRegister(m, len, cudaHostRegisterMapped | cudaHostRegisterPortable) ==
+              cudaSuccess) {
+        p->host_pool = m;
+        p->host_map_len = len;
+        p->host_numa_node = node;
+        return HS_OK;
+      }
+      cudaGetLastError();
+      munmap(m, len);
+    }
+  }
+  const cudaError_t e =
+      cudaHostAlloc(&p->host_pool, p->host_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    p->host_pool = nullptr;
+    return HS_ERR_OOM;
+  }
+  return HS_OK;
 }
 
 template <typename T>
@@ -129,6 +183,13 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
   if (bpl * d.page_tokens > INT32_MAX) return HS_ERR_INVALID;  // row ids are int32
   if ((int64_t)d.max_pages * d.page_tokens > INT32_MAX) return HS_ERR_INVALID;
 
+  {
+    // A host pool larger than this machine's physical memory can never be
+    // pinned: report it before anything is allocated.
+    const long pages = sysconf(_SC_PHYS_PAGES), page = sysconf(_SC_PAGESIZE);
+    const double host_bytes = (double)d.num_layers * (double)d.host_tokens * (double)hs_row_bytes(d);
+    if (pages > 0 && page > 0 && host_bytes > (double)pages * (double)page) return HS_ERR_OOM;
+  }
   hs_pool* p = new (std::nothrow) hs_pool();
   if (!p) return HS_ERR_OOM;
   std::memset(p, 0, sizeof(*p));
@@ -161,14 +222,7 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
   if ((st = dev_alloc(reinterpret_cast<char**>(&p->kv_pool), p->kv_bytes)) != HS_OK) goto fail;
   p->host_bytes = (size_t)L * d.host_tokens * hs_row_bytes(d);
   {
-    cudaError_t e = cudaHostAlloc(&p->host_pool, p->host_bytes,
-                                  cudaHostAllocMapped | cudaHostAllocPortable);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      p->host_pool = nullptr;
-      st = HS_ERR_OOM;
-      goto fail;
-    }
+    if ((st = alloc_host_pool(p)) != HS_OK) goto fail;
     if (cudaHostGetDevicePointer(&p->host_pool_dev, p->host_pool, 0) != cudaSuccess) {
       st = HS_ERR_CUDA;
       goto fail;
@@ -218,6 +272,12 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
 fail:
   free_pool(p);
   return st;
+}
+
+extern "C" hs_status hs_pool_host_numa_node(const hs_pool* p, int32_t* node_out) {
+  if (!p || !node_out) return HS_ERR_INVALID;
+  *node_out = p->host_numa_node;
+  return HS_OK;
 }
 
 extern "C" hs_status hs_pool_destroy(hs_pool* pool) {

@@ -12,7 +12,8 @@ that is all padding; with bf16 and FP8 rows and one, two and many K splits.
 Each case also counts, from the inputs alone, how many heads take the rescale
 under the kernel's work split (``rescale_events``), and asserts that the case
 does reach the path.  Outputs must be within max-abs 1e-2 and mean-rel 2e-3 of
-the fp64 oracle; lse within 2e-3.  Exactness of the method (page
+the fp64 oracle; lse within 2e-3 plus a small part relative to its size
+(the scores here are far larger than the seeded ones).  Exactness of the method (page
 "59188saintaubert.com ... HiSparse", section 02: only placement changes, the
 attention output does not) is what the oracle states.
 """
@@ -37,6 +38,11 @@ D, V_DIM, P = 576, 512, 256
 SCALE = 192 ** -0.5
 LOG2E = 1.4426950408889634
 MAX_ABS, MEAN_REL = 1e-2, 2e-3
+# lse: 2e-3 plus a part relative to its size.  The scores here reach ~200
+# (natural log units) and carry rounding relative to their size: fp32
+# accumulation for bf16 rows; for FP8 rows also the group scale rounded to
+# fp16 (2^-12 relative) in the latent columns.
+LSE_RTOL = {False: 1e-5, True: 2.5e-4}
 
 
 def _bf16(x):
@@ -97,45 +103,52 @@ def rescale_events(s_log2, valid, segments, tile):
 
 def make_case(kind, R, K, H, fp8, seed):
     """Rows in list order for each request, a query per request, and the row ids.
-    kinds:
-      steep     - scores rise by ~10 (log2) every 64 rows along the list
+    The value columns (the first 512) are 0.5 x N(0,1), so every output stays
+    below 2.5 in magnitude, where bf16 output rounding (half an ulp <= 2^-7)
+    leaves room in the 1e-2 bound; the scores move through the 64 rope
+    columns, which enter only the scores.  kinds:
+      steep     - scores rise by ~9 (log2) every 64 rows along the list
       gentle    - scores rise by ~9 (log2) every 256 rows
-      qscale    - seeded N(0,1) rows and queries, the queries times 8
-      dominant  - N(0,1) rows, plus one row aligned with the queries at the end
+      qscale    - rows 0.5 x N(0,1), seeded queries times 16 (scores ~20 log2
+                  wide; times 8 for FP8 rows)
+      dominant  - flat scores, plus one row 40 (log2) above the rest at the end
                   of every 1024-row stretch
       padfirst  - steep, with the first 64 rows of every 1024-row stretch padding
       falling   - steep reversed (the maximum comes first: no rescale needed)
     """
     rng = np.random.default_rng(seed)
-    w = rng.choice([-1.0, 1.0], size=D)
+    w = rng.choice([-1.0, 1.0], size=D - 512)  # rope direction shared by every head
     n_rows = R * K
     vals = np.empty((n_rows, D))
     q = np.empty((R, H, D), dtype=np.uint16)
     valid = np.ones((R, K), dtype=bool)
     per_raw = 1.0 / (SCALE * LOG2E)  # raw score per log2 unit
     for r in range(R):
-        if kind in ("qscale", "dominant"):
+        k = 0.5 * rng.standard_normal((K, D))
+        if kind == "qscale":
+            # FP8 rows reach the score product as fp16 operands (11 significant
+            # bits), whose rounding moves a score by ~2^-12 |q| |k| sqrt(576):
+            # their queries are scaled less (scores ~10 log2 units wide)
             base = synth.bf16_to_f32(synth.q(70 + seed, r, 0, 0, H)).astype(np.float64)
-            if kind == "qscale":
-                q[r] = _bf16(base * 8.0)
-            else:
-                q[r] = _bf16(0.5 * base + w)
-            k = synth.bf16_to_f32(synth.rows(90 + seed, r, 0, 0, K)).astype(np.float64)
-            if kind == "dominant":
-                for j in range(1023, K, 1024):
-                    k[j] = 12.0 * w / math.sqrt(D) + 0.1 * k[j]
-                k[K - 1] = 12.0 * w / math.sqrt(D)
+            q[r] = _bf16(base * (8.0 if fp8 else 16.0))
         else:
-            q[r] = _bf16(w + 0.5 * rng.standard_normal((H, D)))
-            j = np.arange(K, dtype=np.float64)
-            rate = 9.0 / 256.0 if kind == "gentle" else 10.0 / 64.0
-            alpha = rate * j * per_raw / D  # q.k ~ alpha * (q.w) ~ alpha * D
-            if kind == "falling":
-                alpha = alpha[::-1]
-            k = alpha[:, None] * w[None, :] + rng.standard_normal((K, D))
-            if kind == "padfirst":
-                for b in range(0, K, 1024):
-                    valid[r, b:b + 64] = False
+            qf = np.empty((H, D))
+            qf[:, :512] = 0.5 * rng.standard_normal((H, 512))
+            qf[:, 512:] = w
+            q[r] = _bf16(qf)
+            if kind == "dominant":
+                for j in list(range(1023, K, 1024)) + [K - 1]:
+                    k[j, 512:] = 40.0 * per_raw / (D - 512) * w
+            else:
+                j = np.arange(K, dtype=np.float64)
+                rate = 9.0 / 256.0 if kind == "gentle" else 9.0 / 64.0  # log2 units per row
+                a = rate * j * per_raw / (D - 512)  # q.k gains a * 64 from the rope columns
+                if kind == "falling":
+                    a = a[::-1]
+                k[:, 512:] += a[:, None] * w[None, :]
+                if kind == "padfirst":
+                    for b in range(0, K, 1024):
+                        valid[r, b:b + 64] = False
         vals[r * K:(r + 1) * K] = k
     ids = np.arange(n_rows, dtype=np.int32).reshape(R, K)
     ids[~valid] = -1
@@ -191,7 +204,7 @@ def test_attention_with_moving_maximum(kind, R, K, H, fp8):
         err = np.abs(got[r].astype(np.float64) - ref)
         mean_rel = err.sum() / np.abs(ref).sum()
         assert err.max() <= MAX_ABS and mean_rel <= MEAN_REL, (kind, r, err.max(), mean_rel)
-        assert np.allclose(got_lse[r], ref_lse, rtol=0, atol=2e-3), (kind, r)
+        assert np.allclose(got_lse[r], ref_lse, rtol=LSE_RTOL[fp8], atol=2e-3), (kind, r)
         s_log2 = SCALE * LOG2E * (qf[r] @ rows.T)
         events += rescale_events(s_log2, valid[r], segments, tile)
     assert hs.hs_check_errors(pool.handle) == 0

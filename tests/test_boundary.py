@@ -83,3 +83,22 @@ def test_error_codes_match_the_header():
             re.finditer(r"\bHS_(OK|ERR_[A-Z]+)\s*=\s*(-?\d+)", text)}
     for name, value in enum.items():
         assert getattr(hs, "HS_" + name) == value, name
+
+
+def test_unpinnable_host_pool_is_out_of_memory_before_any_allocation():
+    """A host pool larger than the machine's physical memory returns HS_ERR_OOM
+    from the size check, before any CUDA call (so also without a GPU), and
+    leaves the output handle NULL."""
+    import sparse_attention_kv_hs_gb300 as hs
+    lib = hs.load()
+    desc = hs.hs_pool_desc(4, 2, 256, 512, 256, 576, 64, 0, 1 << 40, 4)  # 2 x 2^40 x 1152 B
+    out = ctypes.c_void_p(12345)
+    assert lib.hs_pool_create(ctypes.byref(desc), ctypes.byref(out)) == hs.HS_ERR_OOM
+    assert out.value is None
+
+
+def test_wait_offload_argument_errors_need_no_gpu():
+    import sparse_attention_kv_hs_gb300 as hs
+    lib = hs.load()
+    assert lib.hs_wait_offload(None, 1000) == hs.HS_ERR_INVALID
+    assert lib.hs_wait_offload(ctypes.c_void_p(8), -1) == hs.HS_ERR_INVALID

@@ -106,7 +106,7 @@ def test_noalloc_reports_device_errors_through_its_own_word():
     assert hs.hs_noalloc_check_errors() == hs.DEV_ERR_BLOCK
     got = out.float().cpu().numpy()
     valid = ids2[1] < n
-    o, _ = oracle.sparse_mla_decode(q[1], bad[np.minimum(ids2[1], n - 1)], valid, W.SCALE)
+    o, _ = oracle.sparse_mla_decode(q[1], bad[np.minimum(ids2[1], R * K - 1)], valid, W.SCALE)
     _close(got[1], o, "bad id excluded")
     assert hs.hs_check_errors(pool.handle) == 0  # the pool's own word is untouched
     pool.close()
