@@ -150,6 +150,7 @@ constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((uint32_t)(256 >> 3) << 
                               ((uint32_t)(128 >> 4) << 24);
 
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before giving up
+constexpr uint32_t kSuspendNs = 200;          // longest sleep of one try_wait
 
 struct AttnArgs {
   const uint4* kv;          // this layer's rows: [rows_in_layer][576] bf16 as 16-byte chunks,
@@ -173,25 +174,26 @@ __device__ __forceinline__ uint64_t globaltimer() {
 
 // Bounded wait on a local mbarrier; on timeout (timeout_ns of the global
 // timer, or at once if the CTA is already aborting) returns false, raises the
-// abort flag and sets error bit WAIT.
+// abort flag and sets error bit WAIT.  After one non-blocking probe the thread
+// waits with mbarrier.try_wait, which suspends it until the phase completes
+// (or a hardware time limit passes), so a waiting warp takes no issue slots
+// or shared-memory bandwidth from the warps that do the work.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort,
                                          int32_t* error_word, bool cluster_scope = false,
                                          uint64_t timeout_ns = kWaitNs) {
   if (*abort) return false;
-  uint64_t t0 = 0;
-  for (uint32_t i = 0;; ++i) {
-    const bool ok = cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
-    if (ok) return true;
-    if ((i & 63) == 63) {
-      if (*abort) return false;
-      const uint64_t now = globaltimer();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > timeout_ns) {
-        *abort = 1;
-        atomicOr(error_word, HS_DEV_ERR_WAIT);
-        return false;
-      }
+  if (cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity))
+    return true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    if (cluster_scope ? mbar_try_wait_cluster_hint(bar, parity, kSuspendNs)
+                      : mbar_try_wait_hint(bar, parity, kSuspendNs))
+      return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > timeout_ns) {
+      *abort = 1;
+      atomicOr(error_word, HS_DEV_ERR_WAIT);
+      return false;
     }
   }
 }

@@ -70,10 +70,17 @@ def test_wait_offload_times_out_while_a_host_gate_holds_the_copy():
         gate.wait(20.0)  # bounded: never holds the stream past 20 s
 
     cb = HOSTFN(hold)
+    # streams of their own (the legacy default stream would wait for the gate
+    # itself), and an event that exists before the gate closes
     side = torch.cuda.Stream()
-    main = torch.cuda.current_stream()
-    assert rt.cudaLaunchHostFunc(side.cuda_stream, cb, None) == 0
+    main = torch.cuda.Stream()
     done = torch.cuda.Event()
+    # one offload with the gate open first: the copy kernel's first launch may
+    # load its module, which would wait for a blocked host function
+    hs.hs_offload_prefix(pool.handle, 1, 2, main, side, done)
+    assert hs.hs_wait_offload(done, 10_000_000_000) == hs.HS_OK
+    pool.host_pool[:, 8 * P + 2 * P:8 * P + 3 * P] = 0
+    assert rt.cudaLaunchHostFunc(side.cuda_stream, cb, None) == 0
     hs.hs_offload_prefix(pool.handle, 1, 2, main, side, done)
     try:
         assert entered.wait(10.0)
