@@ -68,7 +68,15 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile", action="store_true",
                     help="small run for profilers: no clocks, no e2e, no CPU baseline")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="attention workload: skip the resolve / gather workload records")
+    ap.add_argument("--extra-steps", type=int, default=40,
+                    help="timed steps of each extra workload record (after 3 warm-up steps)")
+    ap.add_argument("--replica-check", action="store_true",
+                    help="no GPU work: every replica reports its request range and a timing "
+                         "through the same launch, barrier and max-over-ranks path")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-units", default="0:8", help=argparse.SUPPRESS)
     return ap.parse_args(argv)
 
 
@@ -93,6 +101,71 @@ def max_over_ranks(value: float, dist=None, device=None) -> float:
 def weak_scaling_rate(units_per_rank_step: int, steps: int, world: int, elapsed_ms: float) -> float:
     """Whole-job throughput: every rank's units over the slowest rank's time."""
     return world * steps * units_per_rank_step / (elapsed_ms * 1e-3)
+
+
+def dist_context(force_gloo=False):
+    """(dist module or None, world, rank, local rank) of this process; the
+    process group is created once per process (NCCL on GPUs, gloo on CPU)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            backend = "nccl" if (torch.cuda.is_available() and not force_gloo) else "gloo"
+            dist.init_process_group(backend)
+    return dist, world, rank, local
+
+
+def spawn_replicas(args, argv):
+    """`--gpus N` (N > 1) outside torchrun: relaunch this script under
+    torch.distributed.run, one process per GPU on this node (each an
+    independent replica); returns its exit status."""
+    import socket
+    if not args.replica_check:
+        import torch
+        n = torch.cuda.device_count()
+        if args.gpus > n:
+            print(json.dumps({"error": f"--gpus {args.gpus} but {n} GPU(s) visible"}))
+            return 2
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
+
+
+def run_replica_check(args):
+    """Every replica takes its own requests (req_base = rank x R) of the
+    workload and times a CPU stand-in for a step (generating its requests'
+    first selections); rank 0 prints the ranges, world size and the slowest
+    rank's time, through the same barrier / max-over-ranks path as the GPU
+    arm."""
+    dist, world, rank, _ = dist_context(force_gloo=True)
+    w = W.make(args.workload)
+    base = replica_request_base(rank, w.R)
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    w2 = W.Workload(**{**w.__dict__, "steps": 1})
+    w2.req_base = base
+    rows = sum(int((w2.trace(r) >= 0).sum()) for r in range(min(w.R, 2)))
+    ms = max_over_ranks((time.perf_counter() - t0) * 1e3, dist)
+    ranges = [[base, base + w.R]]
+    if dist is not None:
+        got = [None] * world
+        dist.all_gather_object(got, ranges[0])
+        ranges = got
+    if rank == 0:
+        print(json.dumps({"replica_check": True, "n_gpus": world, "scaling": "weak",
+                          "workload": workload_name(w), "requests_per_replica": w.R,
+                          "replica_requests": ranges, "max_rank_ms": ms, "rows": rows}))
+    if dist is not None:
+        dist.destroy_process_group()
 
 
 def load_peaks():
@@ -279,7 +352,7 @@ def ncu_traffic(kernel_file, workload, fp8=False):
 
 # ----------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0, fp8=False):
+def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0, fp8=False, unit0=0):
     """Run the CPU oracle (resolve + gather from host full KV + fp64 attention)
     over the first `units` (request, layer) units of the workload, step after
     step, for about `seconds` after `skip` untimed warm-up steps.  With fp8 the
@@ -294,7 +367,7 @@ def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0, fp8=False):
             o.set_hot_block(r, i, r * w.hot_blocks_per_request() + i)
     for (r, page, blk) in scen.initial:
         o.set_page(r, page, blk)
-    sel = [(u // w.L, u % w.L) for u in range(units)]
+    sel = [(u // w.L, u % w.L) for u in range(unit0, unit0 + units)]
     reqs = sorted({r for r, _ in sel})
     steps = steps_cap or w.steps
     w2 = W.Workload(**{**w.__dict__, "steps": steps})
@@ -320,47 +393,58 @@ def oracle_sample(w, seconds, units=2, steps_cap=None, skip=0, fp8=False):
     return rows_done, time.perf_counter() - t0, t - min(skip, t)
 
 
-def cpu_baseline(w, seconds, fp8=False):
-    """The oracle timed in child processes: with BLAS threads = the host's
-    cores (`value`), and with one thread (`value_1_thread`, a third of the
-    time budget)."""
+def cpu_baseline(w, seconds, fp8=False, units=8):
+    """The oracle timed on the host: `units` (request, layer) units, one child
+    process per unit, all at once (units are independent; each child's BLAS
+    gets an equal share of the cores), for about `seconds`; value = all rows
+    over the slowest child's time.  `value_1_thread`: one unit on one thread."""
     cores = os.cpu_count() or 1
+    procs = min(units, cores)
+    per = max(1, cores // procs)
 
-    def child(threads, secs):
+    def launch(u0, n, threads, secs):
         env = dict(os.environ, OPENBLAS_NUM_THREADS=str(threads), OMP_NUM_THREADS=str(threads),
                    MKL_NUM_THREADS=str(threads))
         cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child",
-               "--workload", w.name, "--cpu-seconds", str(secs),
+               "--workload", w.name, "--cpu-seconds", str(secs), "--cpu-units", f"{u0}:{u0 + n}",
                "--kv-format", "fp8" if fp8 else "bf16"]
-        r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
-        try:
-            return json.loads(r.stdout.strip().splitlines()[-1]), None
-        except Exception:
-            return None, r.stderr[-200:]
+        return subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
+                                env=env)
 
-    d, err = child(cores, seconds)
-    if d is None:
+    def collect(p):
+        try:
+            out, err = p.communicate(timeout=600)
+            return json.loads(out.strip().splitlines()[-1]), None
+        except Exception as e:
+            return None, str(e)[-200:]
+
+    spans = [(i * units // procs, (i + 1) * units // procs - i * units // procs)
+             for i in range(procs)]
+    children = [launch(u0, n, per, seconds) for u0, n in spans]
+    res = [collect(p) for p in children]
+    if any(d is None for d, _ in res):
+        err = next(e for d, e in res if d is None)
         return {"value": None, "unit": "rows/s", "cores": cores, "kind": "oracle",
                 "sample": f"failed: {err}"}
-    d["cores"] = cores
-    d1, _ = child(1, max(seconds / 3, 1.0))
-    d["value_1_thread"] = d1["value"] if d1 else None
-    return d
+    rows = sum(d["rows"] for d, _ in res)
+    secs = max(d["secs"] for d, _ in res)
+    steps = min(d["steps"] for d, _ in res)
+    d1, _ = collect(launch(0, 1, 1, max(seconds / 3, 1.0)))
+    return {"value": rows / secs, "unit": "rows/s", "kind": "oracle", "cores": procs * per,
+            "sample": f"{units} (request, layer) units in {procs} processes x {per} BLAS "
+                      f"threads, >= {steps} steps each (resolve + gather + fp64 attention), "
+                      f"{secs:.1f} s",
+            "value_1_thread": d1["rows"] / d1["secs"] if d1 else None}
 
 
 # ----------------------------------------------------------------- GPU arm
 
 def run_ours(args):
+    """Measure one workload; returns rank 0's JSON line (None on other ranks)."""
     import torch
     import sparse_attention_kv_hs_gb300 as hs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dist, world, rank, local = dist_context()
     torch.cuda.set_device(local)
     lib = hs.load()
 
@@ -581,10 +665,28 @@ def run_ours(args):
         }
         if not args.no_cpu_baseline and not args.profile and world == 1:
             line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, fp8)
-        print(json.dumps(line))
     pool.close()
-    if dist is not None:
-        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def extra_workloads(args):
+    """The resolve and gather workloads at full size, measured in the same run
+    after the attention workload: their rows/s and per-launch rooflines
+    (RESOLVE against the in-run host link peak, the standalone gather against
+    HBM), so the hit/gather-path and miss-path targets are in the same line."""
+    import copy
+    out = {}
+    for name in ("resolve", "gather"):
+        a2 = copy.copy(args)
+        a2.workload, a2.steps, a2.warmup = name, args.extra_steps, 3
+        a2.no_e2e, a2.no_cpu_baseline = True, True
+        rec = run_ours(a2)
+        if rec is not None:
+            out[name] = {k: rec[k] for k in ("value", "unit", "ms_per_step", "steps",
+                                                "miss_rows_per_step", "cold_step", "kernels",
+                                                "host_link_peak_gbs", "clocks", "gpu_launches")}
+            out[name]["workload"] = rec["config"]["workload"]
+    return out
 
 
 def pool_splits(pool, R, K):
@@ -1073,28 +1175,43 @@ def run_reference(args):
 
 
 def main(argv=None):
-    args = parse_args(argv)
+    raw = sys.argv[1:] if argv is None else list(argv)
+    args = parse_args(raw)
     if args.cpu_baseline_child:
         w = W.make(args.workload)
-        rows, secs, steps = oracle_sample(w, args.cpu_seconds, units=8, steps_cap=512,
-                                          fp8=args.kv_format == "fp8")
-        print(json.dumps({"value": rows / secs, "unit": "rows/s", "kind": "oracle",
-                          "sample": f"8 (request, layer) units x {steps} steps "
-                                    f"(resolve + gather + fp64 attention), {secs:.1f} s"}))
-        return
+        u0, u1 = (int(x) for x in args.cpu_units.split(":"))
+        rows, secs, steps = oracle_sample(w, args.cpu_seconds, units=u1 - u0, steps_cap=512,
+                                          fp8=args.kv_format == "fp8", unit0=u0)
+        print(json.dumps({"rows": rows, "secs": secs, "steps": steps}))
+        return 0
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        return spawn_replicas(args, raw)
+    if args.replica_check:
+        run_replica_check(args)
+        return 0
     if args.steps is None:
         args.steps = {"mixed": 120, "spec": 200}.get(args.workload, 2000)
     if args.impl == "reference":
         run_reference(args)
-        return
+        return 0
     if args.workload == "mixed":
         run_mixed(args)
-        return
+        return 0
     if args.workload == "spec":
         run_spec(args)
-        return
-    run_ours(args)
+        return 0
+    line = run_ours(args)
+    if args.workload == "attention" and not args.no_extra and not args.profile:
+        extra = extra_workloads(args)
+        if line is not None:
+            line["workloads"] = extra
+    if line is not None:
+        print(json.dumps(line))
+    dist, _, _, _ = dist_context()
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

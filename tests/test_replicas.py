@@ -50,3 +50,22 @@ def test_single_process_helpers():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.replica_request_base(3, 32) == 96
+
+
+def test_bench_spawns_one_replica_per_gpu_with_disjoint_requests():
+    """`bench.py --gpus 2` outside torchrun relaunches itself as two ranks
+    (gloo here, no GPU work: --replica-check); rank 0 reports both replicas'
+    request ranges, which are disjoint, and n_gpus = 2."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2",
+                        "--replica-check"], capture_output=True, text=True, timeout=300,
+                       cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+    assert line["n_gpus"] == 2 and line["scaling"] == "weak"
+    (a0, a1), (b0, b1) = line["replica_requests"]
+    per = line["requests_per_replica"]
+    assert (a0, a1, b0, b1) == (0, per, per, 2 * per)
