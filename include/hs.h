@@ -130,13 +130,14 @@ typedef struct hs_pool hs_pool; /* opaque, library-owned */
 hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out);
 
 /* The host NUMA node the pool's pinned host pool was placed on, or -1.
- * hs_pool_create places it on the node CUDA reports as nearest the device
- * (preferred-node policy, then registered pinned and mapped), so that on a
- * machine with several sockets each replica's miss reads stay local (page
- * "GLM 5.3 Optimizations, Part 1", section "Composition with the rest of
- * vLLM": one pinned host pool per data-parallel replica); -1 when the device
- * reports no host node or the placement was refused (then cudaHostAlloc
- * placed it). */
+ * On a machine with several host NUMA nodes, hs_pool_create places it on the
+ * node CUDA reports as nearest the device (preferred-node policy, huge pages
+ * where offered, then registered pinned and mapped), so that each replica's
+ * miss reads stay on its socket (page "GLM 5.3 Optimizations, Part 1",
+ * section "Composition with the rest of vLLM": one pinned host pool per
+ * data-parallel replica); -1 with a single node, when the device reports no
+ * host node, or when the placement was refused (then cudaHostAlloc placed
+ * it). */
 hs_status hs_pool_host_numa_node(const hs_pool* pool, int32_t* node_out);
 
 /* Free everything the pool owns.  Synchronises the device first. */

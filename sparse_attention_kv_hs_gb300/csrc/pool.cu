@@ -104,12 +104,25 @@ void free_pool(hs_pool* p) {
   delete p;
 }
 
-// The pinned, mapped host pool, placed on the host NUMA node nearest the
-// device when the system reports one: anonymous memory with that node as the
-// preferred policy (the kernel falls back to other nodes only when it is
-// full), then registered with CUDA (pinned and mapped), so a miss's host read
-// crosses no socket boundary on machines with several.  Where the device has
-// no host NUMA node or the policy call is refused, cudaHostAlloc places it.
+// Host NUMA nodes with memory (node directories under sysfs); 0 if unknown.
+int host_numa_nodes() {
+  int n = 0;
+  for (int i = 0; i < 1024; ++i) {
+    char path[64];
+    snprintf(path, sizeof path, "/sys/devices/system/node/node%d", i);
+    if (access(path, F_OK) == 0) ++n;
+  }
+  return n;
+}
+
+// The pinned, mapped host pool.  On a machine with several host NUMA nodes it
+// is placed on the node CUDA reports as nearest the device: anonymous memory
+// with that node as the preferred policy (the kernel falls back to other
+// nodes only when it is full) and huge pages where the system offers them,
+// then registered with CUDA (pinned and mapped), so a miss's host read
+// crosses no socket boundary.  With one node (or no node reported, or the
+// policy call refused) cudaHostAlloc places it: with nothing to choose, its
+// mapping is the faster one for the GPU's first touch of each page.
 hs_status alloc_host_pool(hs_pool* p) {
   p->host_pool = nullptr;
   p->host_map_len = 0;
@@ -120,10 +133,11 @@ hs_status alloc_host_pool(hs_pool* p) {
     node = -1;
   }
   const long page = sysconf(_SC_PAGESIZE);
-  if (node >= 0 && node < 1024 && page > 0) {
+  if (node >= 0 && node < 1024 && page > 0 && host_numa_nodes() > 1) {
     const size_t len = (p->host_bytes + (size_t)page - 1) / (size_t)page * (size_t)page;
     void* m = mmap(nullptr, len, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
     if (m != MAP_FAILED) {
+      madvise(m, len, MADV_HUGEPAGE);  // advice only: ignored where unsupported
       unsigned long mask[1024 / (8 * sizeof(unsigned long))] = {0};
       mask[node / (8 * sizeof(unsigned long))] |= 1ul << (node % (8 * sizeof(unsigned long)));
       const long kPreferred = 1;  // MPOL_PREFERRED
