@@ -355,7 +355,7 @@ hs_status hs_sparse_mla_decode_tokens(hs_pool* pool, int32_t layer, int32_t num_
  * not meaningful) and INTERNAL (the kernel found its launch set-up unusable
  * and did nothing).
  * It calls no cudaMalloc, cudaFree or other allocating routine: its split-K
- * scratch is a fixed device array of this library (16 MiB + 32 KiB, held by
+ * scratch is a fixed device array of this library (8 MiB + 32 KiB, held by
  * every GPU that loads the library until the process exits), big enough for
  * 64 (request, split) partials; the call uses fewer splits to fit, and returns
  * HS_ERR_INVALID if num_requests x ceil(top_k / 2048) > 64.  The first call on

@@ -33,8 +33,8 @@ struct hs_pool {
   int32_t* error_word;  // scalar
 
   // sparse MLA decode workspace (split-K partials)
-  float* attn_o;    // [R][max_splits][128][512]
-  float* attn_ml;   // [R][max_splits][128] lse
+  uint16_t* attn_o;  // [R][max_splits][128][512] fp16 partials
+  float* attn_ml;    // [R][max_splits][128] lse
   int attn_max_splits;
   void* attn_kv_maps;  // host array of one TMA tensor map per layer (CUtensorMap)
 

@@ -35,7 +35,7 @@
 // (swizzled, then TMEM), each split's row ids are staged in shared memory
 // once, MMA descriptors are computed once and advanced by constants, and
 // every hand-off is an mbarrier.  With several splits per request, each pair
-// writes a normalised fp32 partial and its log-sum-exp; a small merge kernel
+// writes a normalised fp16 partial and its log-sum-exp; a small merge kernel
 // combines them.
 //
 // Every wait is bounded: a wait that times out sets HS_DEV_ERR_WAIT in the
@@ -103,7 +103,7 @@ constexpr uint32_t kPBufBytes = kPBytes + 1024;            // 17408
 // offsets in both CTAs of a pair (the bulk copy and remote barrier operations
 // address the peer by offset).  Swizzled regions are 1024-byte aligned.
 constexpr int kMaxSplitRows = 2048;  // row ids of one split, staged in shared memory
-constexpr uint32_t OFF_STAGE = 0;    // CTA 0 first holds Q here (9 x 16384 B)
+constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // 147456
 constexpr uint32_t OFF_ML = OFF_P + kPBufs * kPBufBytes;       // 217088: m[128], l[128]
 constexpr uint32_t OFF_RID = OFF_ML + 1024;                    // 218112: int32 [2048]
@@ -111,7 +111,18 @@ constexpr uint32_t OFF_BAR = OFF_RID + 4 * kMaxSplitRows;      // 226304
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
 constexpr uint32_t kSmemBytes = OFF_MISC + 64;                 // 226624
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-static_assert(kCbK * kQBlockBytes <= kStages * kStageBytes, "Q must fit the stage region");
+// CTA 0 stages Q (9 column blocks of 16 KB) in two rounds, so that stage 0 is
+// free for the first tile's rows from the start: blocks 0..3 in stage 1 and
+// 4..7 in the P ring, then block 8 in stage 1 once those have moved to TMEM.
+static_assert(kStages == 2 && 4 * kQBlockBytes <= kStageBytes &&
+                  4 * kQBlockBytes <= kPBufs * kPBufBytes && kCbK == 9,
+              "Q staging");
+__host__ __device__ constexpr uint32_t q_block_off(int cb) {
+  return cb < 4 ? OFF_STAGE + kStageBytes + (uint32_t)cb * kQBlockBytes
+         : cb < 8 ? OFF_P + (uint32_t)(cb - 4) * kQBlockBytes
+                  : OFF_STAGE + kStageBytes;
+}
+static_assert(q_block_off(4) % 1024 == 0 && q_block_off(0) % 1024 == 0, "swizzled Q blocks");
 // epilogue staging (4 warps x 8 KiB) reuses the stage region once the last tile is consumed
 static_assert(4 * 8192 <= kStages * kStageBytes, "epilogue staging");
 
@@ -131,7 +142,8 @@ enum {
   B_MMA_IDLE = 23,   // (CTA 1) commit: earlier P.V MMAs finished
   B_ML_FULL = 24,    // (CTA 1) softmax's final m, l -> epilogue
   B_FINAL = 25,      // MMA issuer's last commit
-  B_COUNT = 26
+  B_Q_HALF = 26,     // (CTA 0) softmax warps moved Q blocks 0..7 to TMEM -> Q load
+  B_COUNT = 27
 };
 constexpr int kSBufs = 3;  // S accumulators in TMEM (CTA 0)
 static_assert(B_COUNT * 8 <= 256, "barrier area");
@@ -149,7 +161,7 @@ constexpr uint32_t kIdescS16 = (1u << 4) | ((uint32_t)(kTile >> 3) << 17) |
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((uint32_t)(256 >> 3) << 17) |
                               ((uint32_t)(128 >> 4) << 24);
 
-constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s per wait before giving up
+constexpr uint32_t kWaitNs = 1000000000u;  // 1 s per wait before giving up (< 2^32 ns)
 constexpr uint32_t kSuspendNs = 200;          // longest sleep of one try_wait
 
 struct AttnArgs {
@@ -158,7 +170,7 @@ struct AttnArgs {
   const int32_t* row_ids;   // [R][K]
   uint16_t* out;            // [R][H][512] bf16 (splits == 1)
   float* lse;               // [R][H] or null (splits == 1)
-  float* ws_o;              // [R][splits][128][512] (splits > 1)
+  uint16_t* ws_o;           // [R][splits][128][512] fp16 partials (splits > 1)
   float* ws_lse;            // [R][splits][128]
   int32_t* error_word;
   int32_t rows_in_layer;
@@ -180,17 +192,19 @@ __device__ __forceinline__ uint64_t globaltimer() {
 // or shared-memory bandwidth from the warps that do the work.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort,
                                          int32_t* error_word, bool cluster_scope = false,
-                                         uint64_t timeout_ns = kWaitNs) {
+                                         uint32_t timeout_ns = kWaitNs) {
   if (*abort) return false;
   if (cluster_scope ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity))
     return true;
-  const uint64_t t0 = globaltimer();
+  // the low 32 bits of the timer suffice: they wrap after 4.29 s, longer than
+  // any time limit used here
+  const uint32_t t0 = (uint32_t)globaltimer();
   for (;;) {
     if (cluster_scope ? mbar_try_wait_cluster_hint(bar, parity, kSuspendNs)
                       : mbar_try_wait_hint(bar, parity, kSuspendNs))
       return true;
     if (*abort) return false;
-    if (globaltimer() - t0 > timeout_ns) {
+    if ((uint32_t)globaltimer() - t0 > timeout_ns) {
       *abort = 1;
       atomicOr(error_word, HS_DEV_ERR_WAIT);
       return false;
@@ -198,22 +212,11 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-// Same, for roles run by whole warps: lane 0 polls (one poller per warp keeps
-// the barrier traffic off the shared-memory pipe the MMAs read operands
-// through), then the warp synchronises, which orders lane 0's acquire before
-// every lane's later accesses; every lane gets the same answer, so
-// warp-collective instructions after it are executed uniformly.
-__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, volatile int* abort,
-                                              int32_t* error_word, bool cluster_scope = false) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort, error_word, cluster_scope);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  return ok;
-}
-
-// Same, with every lane polling: for the MMA warp, whose tcgen05 issue
-// (elect.sync) wants the warp converged at all times.
+// Same, for roles run by whole warps: every lane polls and the warp agrees
+// on the answer, so warp-collective instructions after it (tcgen05, shuffles)
+// run uniformly.  (With lane 0 polling alone while the other lanes waited at a
+// shuffle, each hand-off took 0.25-0.5 us longer to be seen: 3 us per call
+// of the 32 x 2048-row workload, 6 us with FP8 rows.)
 __device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, volatile int* abort,
                                              int32_t* error_word, bool cluster_scope = false) {
   const bool ok = wait_bar(bar, parity, abort, error_word, cluster_scope);
@@ -576,8 +579,8 @@ struct Fp8Loader {
   __device__ __forceinline__ static bool overflow(uint32_t vmax) { return f16_overflow(vmax); }
 };
 
-// The loader warps' loop, for any of the loaders above.  The first store waits
-// for q_ready_bar if it is non-zero (Q occupies the stage region until it has
+// The loader warps' loop, for any of the loaders above.  If q_ready_bar is
+// non-zero, the store of tile 1 waits for it (stage 1 holds Q until Q has
 // moved to TMEM).  Returns error bits (VALUE if a value overflowed fp16).
 template <typename Loader>
 __device__ __forceinline__ int load_tiles(const Loader& L, int n_tiles, uint32_t bar_full0,
@@ -587,13 +590,13 @@ __device__ __forceinline__ int load_tiles(const Loader& L, int n_tiles, uint32_t
   bool need_q = q_ready_bar != 0;
   const int lane = threadIdx.x & 31;
   auto put = [&](int t, typename Loader::Regs& v) -> bool {
-    if (need_q) {
-      if (!wait_bar_warp(q_ready_bar, 0, abort_flag, error_word)) return false;
+    if (need_q && t >= 1) {
+      if (!wait_bar_all(q_ready_bar, 0, abort_flag, error_word)) return false;
       need_q = false;
     }
     const int s = t % kStages;
-    if (!wait_bar_warp(bar_empty0 + 8u * s, ((uint32_t)(t / kStages) & 1u) ^ 1u, abort_flag,
-                       error_word))
+    if (!wait_bar_all(bar_empty0 + 8u * s, ((uint32_t)(t / kStages) & 1u) ^ 1u, abort_flag,
+                      error_word))
       return false;
     L.store(t, v, vmax);
     fence_proxy_async_smem();  // generic-proxy stores -> visible to the MMA
@@ -656,6 +659,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_Q_SMEM), 1);
     mbar_init(bar(B_Q_READY), 128);
+    mbar_init(bar(B_Q_HALF), 128);
     mbar_init(bar(B_RID), kLoadWarps);
     mbar_init(bar(B_CORR_REQ), 1);
     mbar_init(bar(B_CORR_DONE), 128);
@@ -677,6 +681,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before any remote operation
+  // The merge kernel (launched as a programmatic dependent) may be scheduled
+  // from now on; its griddepcontrol.wait still waits for this grid to finish
+  // and its writes to be visible.
+  asm volatile("griddepcontrol.launch_dependents;");
   const uint32_t tm = *tmem_holder;
   int err = 0;
 
@@ -724,10 +732,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_RID));
     }
     if (FP8) {
-      // FP8 rows, both CTAs by vector loads: CTA 0 the whole rows (after Q has
-      // left the stage region), CTA 1 the 512 value columns
+      // FP8 rows, both CTAs by vector loads: CTA 0 the whole rows, CTA 1 the
+      // 512 value columns
       const unsigned char* kv8 = reinterpret_cast<const unsigned char*>(a.kv);
-      if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word)) {
+      if (wait_bar_all(bar(B_RID), 0, abort_flag, a.error_word)) {
         if (rank == 0) {
           const Fp8Loader<true> L(kv8, s_rid, sbase + OFF_STAGE, lt, n_tiles);
           err |= load_tiles(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), bar(B_Q_READY),
@@ -742,15 +750,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // CTA 0: the whole 576-column rows by TMA (written straight into the
       // swizzled stage, one shared-memory pass).  Lanes 0..15 of the eight
       // warps issue the 9 x 16 gathers of 4 rows; a row id of -1 reads past the
-      // tensor, which fills zeros.  The first tile waits for Q to leave the
-      // stage region.
+      // tensor, which fills zeros.  Tile 1 waits for Q to leave stage 1.
       const int lw = warp - kLoadWarp0;
-      if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word) &&
-          wait_bar_warp(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
+      if (wait_bar_all(bar(B_RID), 0, abort_flag, a.error_word)) {
         for (int t = 0; t < n_tiles; ++t) {
           const int s = t % kStages;
-          if (!wait_bar_warp(bar(B_KV_EMPTY + s), ((uint32_t)(t / kStages) & 1u) ^ 1u,
-                             abort_flag, a.error_word))
+          if (t == 1 && !wait_bar_all(bar(B_Q_READY), 0, abort_flag, a.error_word)) break;
+          if (!wait_bar_all(bar(B_KV_EMPTY + s), ((uint32_t)(t / kStages) & 1u) ^ 1u,
+                            abort_flag, a.error_word))
             break;
           if (lw == 0 && lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), kStageBytes);
           if (lane < kTile / 4) {
@@ -767,7 +774,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       }
-    } else if (wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word)) {
+    } else if (wait_bar_all(bar(B_RID), 0, abort_flag, a.error_word)) {
       // CTA 1: the 512 value columns by vector loads, converted to fp16
       const ValueLoader L(a.kv, s_rid, sbase + OFF_STAGE, lt);
       err |= load_tiles(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
@@ -778,11 +785,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kQWarp && rank == 0) {
     // ================= Q load (CTA 0) =================
     regs_set<kRegsWG0>();
-    if (lane == 0 && !*abort_flag) {  // Q[r] (128 rows) -> smem by TMA
-      mbar_arrive_expect_tx(bar(B_Q_SMEM), kCbK * kQBlockBytes);
-      for (int cb = 0; cb < kCbK; ++cb)
-        tma_load_2d(sbase + OFF_STAGE + cb * kQBlockBytes, &q_map, cb * 64, r * a.H,
-                    bar(B_Q_SMEM));
+    // Q[r] (128 rows) -> smem by TMA: blocks 0..7, then block 8 into the
+    // space of blocks 0..3 once the softmax warps have moved blocks 0..7
+    if (!*abort_flag) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar(B_Q_SMEM), 8 * kQBlockBytes);
+        for (int cb = 0; cb < 8; ++cb)
+          tma_load_2d(sbase + q_block_off(cb), &q_map, cb * 64, r * a.H, bar(B_Q_SMEM));
+      }
+      __syncwarp();
+      if (wait_bar_all(bar(B_Q_HALF), 0, abort_flag, a.error_word) && lane == 0) {
+        mbar_arrive_expect_tx(bar(B_Q_SMEM), kQBlockBytes);
+        tma_load_2d(sbase + q_block_off(8), &q_map, 8 * 64, r * a.H, bar(B_Q_SMEM));
+      }
     }
     finish();
     return;
@@ -868,15 +883,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     regs_set<kRegsMath>();
     const int h = tid - kMathWarp0 * 32;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = wait_bar_warp(bar(B_Q_SMEM), 0, abort_flag, a.error_word);
-    if (ok) {  // Q[h] -> TMEM columns TM_Q .. TM_Q+287 (pairs), zero for padded heads
-      // swizzled rows: column block cb holds [128 rows][128 B]; 16-byte chunk c
-      // of row h sits at chunk position c ^ (h % 8) (conflict-free reads)
-      const unsigned char* qrow = smem + OFF_STAGE + h * 128;
-      uint32_t qmax = 0;  // bf16 magnitudes seen (FP8 rows: Q must fit fp16)
-      for (int c0 = 0; c0 < kD / 2; c0 += 16) {
+    // Q[h] -> TMEM columns TM_Q .. TM_Q+287 (pairs), zero for padded heads.
+    // Swizzled rows: column block cb holds [128 rows][128 B]; 16-byte chunk c
+    // of row h sits at chunk position c ^ (h % 8) (conflict-free reads).
+    uint32_t qmax = 0;  // bf16 magnitudes seen (FP8 rows: Q must fit fp16)
+    bool ok = wait_bar_all(bar(B_Q_SMEM), 0, abort_flag, a.error_word);
+    for (int round = 0; round < 2; ++round) {  // blocks 0..7, then block 8
+      for (int c0 = round ? 256 : 0; ok && c0 < (round ? kD / 2 : 256); c0 += 16) {
         uint32_t v[16];
-        const unsigned char* blk = qrow + (c0 / 32) * kQBlockBytes;
+        const unsigned char* blk = smem + q_block_off(c0 / 32) + h * 128;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = (c0 % 32) / 4 + i;
@@ -899,12 +914,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tmem_st16(tm + lane_off + TM_Q + c0, v);
       }
+      if (round == 0) {
+        mbar_arrive(bar(B_Q_HALF));  // blocks 0..7 read: block 8 may overwrite 0..3
+        ok = ok && wait_bar_all(bar(B_Q_SMEM), 1, abort_flag, a.error_word);
+      }
+    }
+    if (ok) {
       tmem_st_wait();
       if (FP8 && ValueLoader::overflow(qmax)) err |= HS_DEV_ERR_VALUE;
     }
     tc_fence_before();
     mbar_arrive(bar(B_Q_READY));
-    ok = ok && wait_bar_warp(bar(B_RID), 0, abort_flag, a.error_word);
+    ok = ok && wait_bar_all(bar(B_RID), 0, abort_flag, a.error_word);
     const uint32_t peer_p = mapa(sbase + OFF_P, 1);
     const uint32_t peer_pfull = mapa(bar(B_P_FULL), 1);
     const int wq = warp & 3;  // this warp's heads: 32 wq .. 32 wq + 31
@@ -917,7 +938,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t valid =
           (uint64_t)__ballot_sync(0xffffffffu, s_rid[t * kTile + lane] >= 0) |
           ((uint64_t)__ballot_sync(0xffffffffu, s_rid[t * kTile + lane + 32] >= 0) << 32);
-      if (!wait_bar_warp(bar(B_S_FULL + b), pb, abort_flag, a.error_word)) break;
+      if (!wait_bar_all(bar(B_S_FULL + b), pb, abort_flag, a.error_word)) break;
       tc_fence_after();
       const uint32_t sa = tm + lane_off + TM_S + b * kTile;
       // One read of the tile's 64 scores from tensor memory: the tile max of
@@ -950,7 +971,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m_used = tmax;
       }
       // P buffer t % kPBufs is free once the value CTA finished tile t - kPBufs
-      if (!wait_bar_warp(bar(B_P_EMPTY + pbuf_i), ppar ^ 1u, abort_flag, a.error_word)) break;
+      if (!wait_bar_all(bar(B_P_EMPTY + pbuf_i), ppar ^ 1u, abort_flag, a.error_word)) break;
       unsigned char* pbuf = smem + OFF_P + pbuf_i * kPBufBytes;
       // p = 2^(scale_log2 * x - m_used); invalid rows give p = 0.  m_used is -inf
       // only while no valid row has been seen, and then every p is 0.
@@ -994,8 +1015,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // wait until the value CTA released the last P buffers (its commits landed)
     for (int t = n_tiles - kPBufs; t < n_tiles; ++t) {
       if (t < 0) continue;
-      wait_bar_warp(bar(B_P_EMPTY + t % kPBufs), (uint32_t)(t / kPBufs) & 1u, abort_flag,
-                    a.error_word);
+      wait_bar_all(bar(B_P_EMPTY + t % kPBufs), (uint32_t)(t / kPBufs) & 1u, abort_flag,
+                   a.error_word);
     }
     finish();
     return;
@@ -1006,7 +1027,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;              // this warp's TMEM lane quarter (heads 32wq ..)
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     for (uint32_t k = 0;; ++k) {  // rare: only tiles where some head's max moved
-      if (!wait_bar_warp(bar(B_CORR_REQ), k & 1u, abort_flag, a.error_word)) break;
+      if (!wait_bar_all(bar(B_CORR_REQ), k & 1u, abort_flag, a.error_word)) break;
       if (*corr_exit) break;
       tc_fence_after();
       const int t = *corr_tile;
@@ -1040,8 +1061,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     // epilogue: O / l, 64 columns at a time, through this warp's 8 KiB of the
     // (now idle) stage region so that the global stores are whole rows
-    bool ok = wait_bar_warp(bar(B_FINAL), 0, abort_flag, a.error_word) && n_tiles > 0;
-    const bool have_ml = wait_bar_warp(bar(B_ML_FULL), 0, abort_flag, a.error_word, true);
+    bool ok = wait_bar_all(bar(B_FINAL), 0, abort_flag, a.error_word) && n_tiles > 0;
+    const bool have_ml = wait_bar_all(bar(B_ML_FULL), 0, abort_flag, a.error_word, true);
     ok = ok && have_ml;  // warp-uniform: gates the warp-collective TMEM loads below
     tc_fence_after();
     const float m = have_ml ? reinterpret_cast<const float*>(smem + OFF_ML)[h] : -INFINITY;
@@ -1050,6 +1071,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float inv_l = has_rows ? 1.f / l : 0.f;
     const float lse = has_rows ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
     const uint32_t stg = sbase + OFF_STAGE + (uint32_t)wq * 8192u;
+    // One split: the bf16 output.  Several: this split's partial O / l in fp16
+    // (|O / l| is at most the largest |value|, which the loaders hold below
+    // 65536, so fp16 keeps it; 11 significant bits, against bf16's 8 in the
+    // final output) for the merge kernel.  Both are 16-bit: 64 B per head per
+    // 32 columns.
+    const bool partial = a.splits > 1;
+    uint16_t* dst = partial ? a.ws_o + (((int64_t)r * a.splits + split) * kHeads + wq * 32) * kDV
+                            : a.out + ((int64_t)r * a.H + wq * 32) * kDV;
     for (int c0 = 0; c0 < kDV; c0 += 32) {  // 32 columns at a time (few live registers)
       uint32_t u[32];
       if (ok) {
@@ -1058,51 +1087,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld16p(oa + 16, u + 16);
         tmem_ld_wait();
       }
-      if (a.splits == 1) {
-        // bf16: a head's 32 columns are 4 chunks of 16 B, chunk k at k ^ (lane % 4)
+      // a head's 32 columns are 4 chunks of 16 B, chunk k at k ^ (lane % 4)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t pk[4];
+      for (int k = 0; k < 4; ++k) {
+        uint32_t pk[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            pk[i] = has_rows ? pack_bf16x2(__uint_as_float(u[8 * k + 2 * i]) * inv_l,
-                                           __uint_as_float(u[8 * k + 2 * i + 1]) * inv_l)
-                             : 0u;
-          st_shared_v4(stg + lane * 64 + ((k ^ (lane & 3)) << 4),
-                       make_uint4(pk[0], pk[1], pk[2], pk[3]));
+        for (int i = 0; i < 4; ++i) {
+          const float x = __uint_as_float(u[8 * k + 2 * i]) * inv_l;
+          const float y = __uint_as_float(u[8 * k + 2 * i + 1]) * inv_l;
+          pk[i] = !has_rows ? 0u : partial ? pack_f16x2(x, y) : pack_bf16x2(x, y);
         }
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {  // 8 heads x 64 B per instruction
-          const int row = 8 * i + (lane >> 2), k = lane & 3;
-          const uint4 v = ld_shared_v4(stg + row * 64 + ((k ^ (row & 3)) << 4));
-          const int head = wq * 32 + row;
-          if (head < a.H)
-            *reinterpret_cast<uint4*>(a.out + ((int64_t)r * a.H + head) * kDV + c0 + 8 * k) = v;
-        }
-        __syncwarp();
-      } else {
-        // fp32: 8 chunks of 16 B per head, chunk k at k ^ (lane % 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (has_rows)
-            v = make_uint4(__float_as_uint(__uint_as_float(u[4 * k]) * inv_l),
-                           __float_as_uint(__uint_as_float(u[4 * k + 1]) * inv_l),
-                           __float_as_uint(__uint_as_float(u[4 * k + 2]) * inv_l),
-                           __float_as_uint(__uint_as_float(u[4 * k + 3]) * inv_l));
-          st_shared_v4(stg + lane * 128 + ((k ^ (lane & 7)) << 4), v);
-        }
-        __syncwarp();
-        float* wo = a.ws_o + (((int64_t)r * a.splits + split) * kHeads + wq * 32) * kDV + c0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {  // 4 heads x 128 B per instruction
-          const int row = 4 * i + (lane >> 3), k = lane & 7;
-          const uint4 v = ld_shared_v4(stg + row * 128 + ((k ^ (row & 7)) << 4));
-          *reinterpret_cast<uint4*>(wo + (int64_t)row * kDV + 4 * k) = v;
-        }
-        __syncwarp();
+        st_shared_v4(stg + lane * 64 + ((k ^ (lane & 3)) << 4),
+                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
       }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // 8 heads x 64 B per instruction
+        const int row = 8 * i + (lane >> 2), k = lane & 3;
+        const uint4 v = ld_shared_v4(stg + row * 64 + ((k ^ (row & 3)) << 4));
+        if (wq * 32 + row < a.H)
+          *reinterpret_cast<uint4*>(dst + (int64_t)row * kDV + c0 + 8 * k) = v;
+      }
+      __syncwarp();
     }
     if (a.splits == 1) {
       if (h < a.H && a.lse) a.lse[(int64_t)r * a.H + h] = lse;
@@ -1118,11 +1124,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-// Combine per-split normalised partials: o = sum_c w_c o_c / sum_c w_c with
-// w_c = exp(lse_c - max lse).  One CTA per (request, head), 128 threads x 4.
 // Self-test of wait_bar's time limit: one thread waits on a barrier of its
 // CTA that nothing arrives on, and gives up after timeout_ns.
-__global__ void wait_selftest_kernel(int32_t* error_word, uint64_t timeout_ns) {
+__global__ void wait_selftest_kernel(int32_t* error_word, uint32_t timeout_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -1133,29 +1137,37 @@ __global__ void wait_selftest_kernel(int32_t* error_word, uint64_t timeout_ns) {
   if (threadIdx.x == 0) wait_bar(smem_u32(&bar), 0, &abort_flag, error_word, false, timeout_ns);
 }
 
-__global__ void __launch_bounds__(128) merge_splits_kernel(const float* __restrict__ ws_o,
-                                                           const float* __restrict__ ws_lse,
-                                                           int splits, int H,
-                                                           uint16_t* __restrict__ out,
-                                                           float* __restrict__ lse_out) {
-  const int r = blockIdx.y, h = blockIdx.x;
-  const int e0 = threadIdx.x * 4;
+// Combine per-split normalised partials: o = sum_c w_c o_c / sum_c w_c with
+// w_c = exp(lse_c - max lse).  A CTA covers four heads of one request, 64
+// threads per head, each thread 8 columns (one 16-byte fp16 load per split).
+constexpr int kMergeHeads = 4;
+__global__ void __launch_bounds__(64 * kMergeHeads) merge_splits_kernel(
+    const uint16_t* __restrict__ ws_o, const float* __restrict__ ws_lse, int splits, int H,
+    uint16_t* __restrict__ out, float* __restrict__ lse_out) {
+  // launched as a programmatic dependent of the decode kernel: wait for that
+  // grid to complete and its partials to be visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int r = blockIdx.y, h = blockIdx.x * kMergeHeads + (threadIdx.x >> 6);
+  if (h >= H) return;
+  const int e0 = (threadIdx.x & 63) * 8;
   const float* lse_rh = ws_lse + (int64_t)r * splits * kHeads + h;
-  const float* o_rh = ws_o + ((int64_t)r * splits * kHeads + h) * kDV + e0;
+  const uint16_t* o_rh = ws_o + ((int64_t)r * splits * kHeads + h) * kDV + e0;
   // Splits in groups of four, each group's loads issued together: a running
   // max with the sums rescaled when it grows (with at most four splits, one
   // group: the plain max-then-weights sum).
   float mx = -INFINITY, wsum = 0.f;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   for (int c0 = 0; c0 < splits; c0 += 4) {
     float lc[4];
-    float4 o[4];
+    uint4 o[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int c = c0 + u;
       lc[u] = c < splits ? lse_rh[(int64_t)c * kHeads] : -INFINITY;
-      o[u] = c < splits ? *reinterpret_cast<const float4*>(o_rh + (int64_t)c * kHeads * kDV)
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      o[u] = c < splits ? __ldg(reinterpret_cast<const uint4*>(o_rh + (int64_t)c * kHeads * kDV))
+                        : make_uint4(0u, 0u, 0u, 0u);
     }
     float m_new = mx;
 #pragma unroll
@@ -1164,25 +1176,30 @@ __global__ void __launch_bounds__(128) merge_splits_kernel(const float* __restri
       const float k = expf(mx - m_new);
       wsum *= k;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] *= k;
+      for (int i = 0; i < 8; ++i) acc[i] *= k;
     }
     mx = m_new;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const float w = lc[u] == -INFINITY ? 0.f : expf(lc[u] - mx);
       wsum += w;
-      acc[0] += w * o[u].x;
-      acc[1] += w * o[u].y;
-      acc[2] += w * o[u].z;
-      acc[3] += w * o[u].w;
+      const uint32_t wd[4] = {o[u].x, o[u].y, o[u].z, o[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wd[i]));
+        acc[2 * i] += w * f.x;
+        acc[2 * i + 1] += w * f.y;
+      }
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint2 pk;
+  uint4 pk;
   pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
   pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-  *reinterpret_cast<uint2*>(out + ((int64_t)r * H + h) * kDV + e0) = pk;
-  if (lse_out && threadIdx.x == 0)
+  pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(out + ((int64_t)r * H + h) * kDV + e0) = pk;
+  if (lse_out && (threadIdx.x & 63) == 0)
     lse_out[(int64_t)r * H + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
 }
 
@@ -1241,8 +1258,19 @@ hs_status launch_decode(AttnArgs& a, const CUtensorMap& kv_map, const void* q, i
     mla_decode_kernel<false><<<dim3(2 * a.splits, R), kThreads, kSmemBytes, s>>>(kv_map, q_map, a);
   HS_CUDA_TRY(cudaGetLastError());
   if (a.splits > 1) {
-    merge_splits_kernel<<<dim3(a.H, R), 128, 0, s>>>(a.ws_o, a.ws_lse, a.splits, a.H, a.out,
-                                                     a.lse);
+    // programmatic dependent launch: the merge grid is set up while the
+    // decode kernel runs (1.5 us per call of 32 requests x 2048 rows)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.H + kMergeHeads - 1) / kMergeHeads, R);
+    cfg.blockDim = dim3(64 * kMergeHeads);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, merge_splits_kernel, (const uint16_t*)a.ws_o,
+                                   (const float*)a.ws_lse, a.splits, a.H, a.out, a.lse));
     HS_CUDA_TRY(cudaGetLastError());
   }
   return HS_OK;
@@ -1285,7 +1313,7 @@ hs_status hs_attn_workspace_init(hs_pool* p) {
   p->attn_max_splits = splits;
   if (splits > 1) {
     const size_t n = (size_t)p->d.num_requests * splits * kHeads;
-    if (cudaMalloc(&p->attn_o, n * kDV * sizeof(float)) != cudaSuccess ||
+    if (cudaMalloc(&p->attn_o, n * kDV * sizeof(uint16_t)) != cudaSuccess ||
         cudaMalloc(&p->attn_ml, n * sizeof(float)) != cudaSuccess) {
       cudaGetLastError();
       return HS_ERR_OOM;
@@ -1378,7 +1406,7 @@ extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int3
 // or a plug-in that only receives raw device pointers from its host.  For
 // them, hs_sparse_mla_decode_noalloc() takes the KV rows, queries, row ids and
 // outputs as plain pointers and keeps its split-K scratch (per-split partial
-// outputs and their log-sum-exp) in the fixed device array below, which every
+// outputs and their log-sum-exp) in the fixed device arrays below, which every
 // GPU that loads this library holds until the process exits.  It calls no
 // cudaMalloc, cudaFree or allocating library routine.
 //
@@ -1389,13 +1417,15 @@ extern "C" hs_status hs_sparse_mla_decode_tokens(hs_pool* p, int32_t layer, int3
 // Every call overwrites the scratch it uses before reading it, so nothing has
 // to start at zero; calls whose kernels overlap on the GPU (e.g. on two
 // streams) share the array and race.
-constexpr int kNoAllocMaxUnits = 64;  // 64 x 128 x 512 fp32 = 16 MiB (+ 32 KiB lse)
-static __device__ __align__(256) float g_noalloc_scratch[kNoAllocMaxUnits * kHeads * (kDV + 1)];
+constexpr int kNoAllocMaxUnits = 64;  // 64 x 128 x 512 fp16 = 8 MiB, + 32 KiB of lse
+static __device__ __align__(256) uint16_t g_noalloc_o[kNoAllocMaxUnits * kHeads * kDV];
+static __device__ __align__(256) float g_noalloc_lse[kNoAllocMaxUnits * kHeads];
 static __device__ int32_t g_noalloc_error_word;
 
 namespace {
 constexpr int kMaxDevices = 64;
-float* g_noalloc_ptr[kMaxDevices];       // device address of the scratch, per device
+uint16_t* g_noalloc_o_ptr[kMaxDevices];  // device addresses of the scratch, per device
+float* g_noalloc_lse_ptr[kMaxDevices];
 int32_t* g_noalloc_err_ptr[kMaxDevices];
 int g_noalloc_sms[kMaxDevices];
 
@@ -1403,10 +1433,12 @@ int g_noalloc_sms[kMaxDevices];
 // address (in host code the array's name is only a stand-in, not an address)
 // and raise the kernel's shared-memory limit.
 hs_status noalloc_setup(int dev) {
-  if (g_noalloc_ptr[dev]) return HS_OK;
-  void* scratch = nullptr;
+  if (g_noalloc_o_ptr[dev]) return HS_OK;
+  void* scratch_o = nullptr;
+  void* scratch_lse = nullptr;
   void* errw = nullptr;
-  HS_CUDA_TRY(cudaGetSymbolAddress(&scratch, g_noalloc_scratch));
+  HS_CUDA_TRY(cudaGetSymbolAddress(&scratch_o, g_noalloc_o));
+  HS_CUDA_TRY(cudaGetSymbolAddress(&scratch_lse, g_noalloc_lse));
   HS_CUDA_TRY(cudaGetSymbolAddress(&errw, g_noalloc_error_word));
   HS_CUDA_TRY(cudaFuncSetAttribute(mla_decode_kernel<false>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
@@ -1414,7 +1446,8 @@ hs_status noalloc_setup(int dev) {
   HS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   g_noalloc_sms[dev] = sms;
   g_noalloc_err_ptr[dev] = static_cast<int32_t*>(errw);
-  g_noalloc_ptr[dev] = static_cast<float*>(scratch);
+  g_noalloc_lse_ptr[dev] = static_cast<float*>(scratch_lse);
+  g_noalloc_o_ptr[dev] = static_cast<uint16_t*>(scratch_o);
   return HS_OK;
 }
 }  // namespace
@@ -1446,14 +1479,13 @@ extern "C" hs_status hs_sparse_mla_decode_noalloc(const void* kv_rows, int64_t n
   if (splits < min_splits) splits = min_splits;
   CUtensorMap kv_map;  // host-side encode only
   if (encode_rows_map(&kv_map, kv_rows, (uint64_t)num_rows, 1) != HS_OK) return HS_ERR_INVALID;
-  float* scratch = g_noalloc_ptr[dev];
   AttnArgs a;
   a.kv = static_cast<const uint4*>(kv_rows);
   a.row_ids = row_ids;
   a.out = static_cast<uint16_t*>(out);
   a.lse = lse;
-  a.ws_o = scratch;
-  a.ws_lse = scratch + (size_t)kNoAllocMaxUnits * kHeads * kDV;
+  a.ws_o = g_noalloc_o_ptr[dev];
+  a.ws_lse = g_noalloc_lse_ptr[dev];
   a.error_word = g_noalloc_err_ptr[dev];
   a.rows_in_layer = (int32_t)num_rows;
   a.K = top_k;
@@ -1482,7 +1514,7 @@ extern "C" hs_status hs_selftest_bounded_waits(int64_t timeout_ns, int32_t* resu
   if (!result || timeout_ns <= 0 || timeout_ns > 100000000) return HS_ERR_INVALID;
   cudaStream_t st = hs_stream(stream);
   HS_CUDA_TRY(cudaMemsetAsync(result, 0, 2 * sizeof(int32_t), st));
-  wait_selftest_kernel<<<1, 32, 0, st>>>(result, (uint64_t)timeout_ns);
+  wait_selftest_kernel<<<1, 32, 0, st>>>(result, (uint32_t)timeout_ns);
   HS_CUDA_TRY(cudaGetLastError());
   return hs_launch_peer_wait_selftest(result + 1, (uint64_t)timeout_ns, st);
 }
