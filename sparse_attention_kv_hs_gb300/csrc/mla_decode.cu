@@ -62,7 +62,11 @@ constexpr int kHeads = 128;        // MMA M (heads, zero-padded)
 constexpr int kD = 576;            // row width (latent 512 + rope 64)
 constexpr int kDV = 512;           // value width
 constexpr int kTile = 64;          // KV rows per tile
-constexpr int kStages = 2;         // KV tile ring depth
+// KV tile ring depth: 3 in the score CTA (a stage is held from its gathers'
+// issue, ~2 us of TMA latency, through its score MMA, so two stages kept the
+// gathers idle a third of the time), 2 in the value CTA (whose loader threads
+// hold two more tiles in registers)
+constexpr int kStagesS = 3, kStagesV = 2;
 constexpr int kThreads = 512;
 // Warp roles (four warpgroups of four warps):
 //   warp 0       MMA issuer               warp 1 (CTA 0)  Q load
@@ -89,61 +93,58 @@ constexpr uint32_t kBlockBytes = kTile * 128;              // one column block o
 constexpr uint32_t kStageBytes = kCbK * kBlockBytes;       // 73728
 constexpr uint32_t kQBlockBytes = kHeads * 128;            // 16384
 constexpr uint32_t kPBytes = kHeads * kTile * 2;           // 16384 (fp16)
-// P buffer: P [128 heads x 64 rows] fp16, then alpha[128] (fp32), then one
-// 16-byte flag record per softmax warp.  Each softmax warp sends its own 32
-// heads' slice (4096 B of P, 128 B of alpha, its flag record) by bulk copy.
+// P buffer (value CTA): P [128 heads x 64 rows] fp16, then alpha[128] (fp32),
+// then one 16-byte flag record per softmax warp.  The softmax threads store
+// them from registers into the value CTA's buffer (st.async, counted by the
+// buffer's barrier): a head's 128 B of P and its alpha, and each warp's flag.
 constexpr int kPBufs = 4;                                  // P ring depth
-constexpr uint32_t kPWarpBytes = kPBytes / 4;              // 4096
 constexpr uint32_t kPAlphaOff = kPBytes;                   // alpha[128]
 constexpr uint32_t kPFlagOff = kPBytes + 512;              // 4 x 16-byte flag records
-constexpr uint32_t kPCopyBytes = 4 * (kPWarpBytes + 128 + 16);  // 16960 per tile
+constexpr uint32_t kPCopyBytes = kHeads * (kTile * 2 + 4) + 4 * 16;  // 16960 per tile
 constexpr uint32_t kPBufBytes = kPBytes + 1024;            // 17408
 
-// Shared-memory layout.  The P buffers, m/l and the barriers sit at the same
-// offsets in both CTAs of a pair (the bulk copy and remote barrier operations
-// address the peer by offset).  Swizzled regions are 1024-byte aligned.
+// Shared-memory layout.  The score CTA holds 3 K stages; the value CTA 2 V
+// stages, the P ring and m/l in the same bytes.  Row ids, barriers and the
+// scalars sit at the same offsets in both CTAs (remote barrier operations
+// address the peer by offset), as do the value CTA's P buffers and m/l, which
+// the score CTA writes.  Swizzled regions are 1024-byte aligned.
 constexpr int kMaxSplitRows = 2048;  // row ids of one split, staged in shared memory
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_P = OFF_STAGE + kStages * kStageBytes;  // 147456
-constexpr uint32_t OFF_ML = OFF_P + kPBufs * kPBufBytes;       // 217088: m[128], l[128]
-constexpr uint32_t OFF_RID = OFF_ML + 1024;                    // 218112: int32 [2048]
-constexpr uint32_t OFF_BAR = OFF_RID + 4 * kMaxSplitRows;      // 226304
+constexpr uint32_t OFF_P = OFF_STAGE + kStagesV * kStageBytes;  // 147456 (value CTA)
+constexpr uint32_t OFF_ML = OFF_P + kPBufs * kPBufBytes;        // 217088: m[128], l[128]
+constexpr uint32_t OFF_RID = OFF_STAGE + kStagesS * kStageBytes;  // 221184: int32 [2048]
+constexpr uint32_t OFF_BAR = OFF_RID + 4 * kMaxSplitRows;       // 229376
 constexpr uint32_t OFF_MISC = OFF_BAR + 256;
-constexpr uint32_t kSmemBytes = OFF_MISC + 64;                 // 226624
+constexpr uint32_t kSmemBytes = OFF_MISC + 64;                  // 229696
 static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-// CTA 0 stages Q (9 column blocks of 16 KB) in two rounds, so that stage 0 is
-// free for the first tile's rows from the start: blocks 0..3 in stage 1 and
-// 4..7 in the P ring, then block 8 in stage 1 once those have moved to TMEM.
-static_assert(kStages == 2 && 4 * kQBlockBytes <= kStageBytes &&
-                  4 * kQBlockBytes <= kPBufs * kPBufBytes && kCbK == 9,
-              "Q staging");
+static_assert(OFF_ML + 1024 <= OFF_RID, "value CTA layout");
+// CTA 0 stages Q (9 column blocks of 16 KB) in stages 1 and 2, so that stage 0
+// is free for the first tile's rows from the start.
+static_assert(kStagesS == 3 && kCbK * kQBlockBytes == 2 * kStageBytes, "Q staging");
 __host__ __device__ constexpr uint32_t q_block_off(int cb) {
-  return cb < 4 ? OFF_STAGE + kStageBytes + (uint32_t)cb * kQBlockBytes
-         : cb < 8 ? OFF_P + (uint32_t)(cb - 4) * kQBlockBytes
-                  : OFF_STAGE + kStageBytes;
+  return OFF_STAGE + kStageBytes + (uint32_t)cb * kQBlockBytes;
 }
-static_assert(q_block_off(4) % 1024 == 0 && q_block_off(0) % 1024 == 0, "swizzled Q blocks");
+static_assert(q_block_off(0) % 1024 == 0 && kQBlockBytes % 1024 == 0, "swizzled Q blocks");
 // epilogue staging (4 warps x 8 KiB) reuses the stage region once the last tile is consumed
-static_assert(4 * 8192 <= kStages * kStageBytes, "epilogue staging");
+static_assert(4 * 8192 <= kStagesV * kStageBytes, "epilogue staging");
 
 // barrier indices (8 bytes each at OFF_BAR)
 enum {
-  B_KV_FULL = 0,     // [2] loader warps stored a tile -> MMA (both CTAs: K tile / V tile)
-  B_KV_EMPTY = 2,    // [2] MMA commit -> loaders
-  B_S_FULL = 4,      // [3] score MMA commit -> softmax
-  B_S_EMPTY = 7,     // [3] softmax -> score MMA
-  B_P_EMPTY = 10,    // [4] (CTA 0) value MMA commit (multicast) -> softmax
-  B_P_FULL = 14,     // [4] (CTA 1) bulk copies complete_tx -> value MMA
-  B_Q_SMEM = 18,     // (CTA 0) TMA of Q landed in shared memory
-  B_Q_READY = 19,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loaders
-  B_RID = 20,        // loader warps staged this split's row ids
-  B_CORR_REQ = 21,   // (CTA 1) value MMA -> rescale warps
-  B_CORR_DONE = 22,  // (CTA 1) rescale warps -> value MMA
-  B_MMA_IDLE = 23,   // (CTA 1) commit: earlier P.V MMAs finished
-  B_ML_FULL = 24,    // (CTA 1) softmax's final m, l -> epilogue
-  B_FINAL = 25,      // MMA issuer's last commit
-  B_Q_HALF = 26,     // (CTA 0) softmax warps moved Q blocks 0..7 to TMEM -> Q load
-  B_COUNT = 27
+  B_KV_FULL = 0,     // [3] loader warps stored a tile -> MMA (both CTAs: K tile / V tile)
+  B_KV_EMPTY = 3,    // [3] MMA commit -> loaders
+  B_S_FULL = 6,      // [3] score MMA commit -> softmax
+  B_S_EMPTY = 9,     // [3] softmax -> score MMA
+  B_P_EMPTY = 12,    // [4] (CTA 0) value MMA commit (multicast) -> softmax
+  B_P_FULL = 16,     // [4] (CTA 1) the softmax's remote stores complete_tx -> value MMA
+  B_Q_SMEM = 20,     // (CTA 0) TMA of Q landed in shared memory
+  B_Q_READY = 21,    // (CTA 0) softmax warps put Q in TMEM -> score MMA, loaders
+  B_RID = 22,        // loader warps staged this split's row ids
+  B_CORR_REQ = 23,   // (CTA 1) value MMA -> rescale warps
+  B_CORR_DONE = 24,  // (CTA 1) rescale warps -> value MMA
+  B_MMA_IDLE = 25,   // (CTA 1) commit: earlier P.V MMAs finished
+  B_ML_FULL = 26,    // (CTA 1) softmax's final m, l -> epilogue
+  B_FINAL = 27,      // MMA issuer's last commit
+  B_COUNT = 28
 };
 constexpr int kSBufs = 3;  // S accumulators in TMEM (CTA 0)
 static_assert(B_COUNT * 8 <= 256, "barrier area");
@@ -325,6 +326,7 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
 // The bf16 values are converted to fp16 on the way.  A row id of -1 stores
 // zeros.
 struct ValueLoader {
+  static constexpr int kNst = kStagesV;  // stage ring depth (value CTA)
   struct Regs {
     uint4 v[16];
   };
@@ -354,7 +356,7 @@ struct ValueLoader {
     }
   }
   __device__ __forceinline__ void store(int t, Regs& R, uint32_t& vmax) const {
-    const uint32_t stage = stage0 + (uint32_t)(t % kStages) * kStageBytes;
+    const uint32_t stage = stage0 + (uint32_t)(t % kNst) * kStageBytes;
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       uint4 x = R.v[k];
@@ -442,6 +444,7 @@ __device__ __forceinline__ bool f16_overflow(uint32_t vmax) {
 // positions in every store).
 template <bool ROPE>
 struct Fp8Loader {
+  static constexpr int kNst = ROPE ? kStagesS : kStagesV;  // score CTA : value CTA
   struct Regs {
     uint4 lat[2][4];
     uint4 sc[2];
@@ -501,7 +504,7 @@ struct Fp8Loader {
   // rounding to fp16) with a range check of every value.
   template <bool FAST>
   __device__ __forceinline__ void store_rows(int t, Regs& R, uint32_t& vmax) const {
-    const uint32_t stage = stage0 + (uint32_t)(t % kStages) * kStageBytes;
+    const uint32_t stage = stage0 + (uint32_t)(t % kNst) * kStageBytes;
     uint32_t nan0 = 0, nan1 = 0;  // NaN-propagating maxima (fp16x2)
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
@@ -580,8 +583,8 @@ struct Fp8Loader {
 };
 
 // The loader warps' loop, for any of the loaders above.  If q_ready_bar is
-// non-zero, the store of tile 1 waits for it (stage 1 holds Q until Q has
-// moved to TMEM).  Returns error bits (VALUE if a value overflowed fp16).
+// non-zero, the store of tile 1 waits for it (stages 1 and 2 hold Q until Q
+// has moved to TMEM).  Returns error bits (VALUE if a value overflowed fp16).
 template <typename Loader>
 __device__ __forceinline__ int load_tiles(const Loader& L, int n_tiles, uint32_t bar_full0,
                                           uint32_t bar_empty0, uint32_t q_ready_bar,
@@ -594,8 +597,9 @@ __device__ __forceinline__ int load_tiles(const Loader& L, int n_tiles, uint32_t
       if (!wait_bar_all(q_ready_bar, 0, abort_flag, error_word)) return false;
       need_q = false;
     }
-    const int s = t % kStages;
-    if (!wait_bar_all(bar_empty0 + 8u * s, ((uint32_t)(t / kStages) & 1u) ^ 1u, abort_flag,
+    constexpr int kNst = Loader::kNst;
+    const int s = t % kNst;
+    if (!wait_bar_all(bar_empty0 + 8u * s, ((uint32_t)(t / kNst) & 1u) ^ 1u, abort_flag,
                       error_word))
       return false;
     L.store(t, v, vmax);
@@ -644,7 +648,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, tensor memory ---------------------------------
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < (rank == 0 ? kStagesS : kStagesV); ++i) {
       // TMA (CTA 0, bf16 rows): one arm (+ the bytes); else one arrival per loader warp
       mbar_init(bar(B_KV_FULL + i), (rank == 0 && !FP8) ? 1 : kLoadWarps);
       mbar_init(bar(B_KV_EMPTY + i), 1);
@@ -659,7 +663,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_Q_SMEM), 1);
     mbar_init(bar(B_Q_READY), 128);
-    mbar_init(bar(B_Q_HALF), 128);
     mbar_init(bar(B_RID), kLoadWarps);
     mbar_init(bar(B_CORR_REQ), 1);
     mbar_init(bar(B_CORR_DONE), 128);
@@ -750,13 +753,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // CTA 0: the whole 576-column rows by TMA (written straight into the
       // swizzled stage, one shared-memory pass).  Lanes 0..15 of the eight
       // warps issue the 9 x 16 gathers of 4 rows; a row id of -1 reads past the
-      // tensor, which fills zeros.  Tile 1 waits for Q to leave stage 1.
+      // tensor, which fills zeros.  Tile 1 waits for Q to leave stages 1-2.
       const int lw = warp - kLoadWarp0;
       if (wait_bar_all(bar(B_RID), 0, abort_flag, a.error_word)) {
         for (int t = 0; t < n_tiles; ++t) {
-          const int s = t % kStages;
+          const int s = t % kStagesS;
           if (t == 1 && !wait_bar_all(bar(B_Q_READY), 0, abort_flag, a.error_word)) break;
-          if (!wait_bar_all(bar(B_KV_EMPTY + s), ((uint32_t)(t / kStages) & 1u) ^ 1u,
+          if (!wait_bar_all(bar(B_KV_EMPTY + s), ((uint32_t)(t / kStagesS) & 1u) ^ 1u,
                             abort_flag, a.error_word))
             break;
           if (lw == 0 && lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), kStageBytes);
@@ -785,19 +788,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kQWarp && rank == 0) {
     // ================= Q load (CTA 0) =================
     regs_set<kRegsWG0>();
-    // Q[r] (128 rows) -> smem by TMA: blocks 0..7, then block 8 into the
-    // space of blocks 0..3 once the softmax warps have moved blocks 0..7
-    if (!*abort_flag) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(B_Q_SMEM), 8 * kQBlockBytes);
-        for (int cb = 0; cb < 8; ++cb)
-          tma_load_2d(sbase + q_block_off(cb), &q_map, cb * 64, r * a.H, bar(B_Q_SMEM));
-      }
-      __syncwarp();
-      if (wait_bar_all(bar(B_Q_HALF), 0, abort_flag, a.error_word) && lane == 0) {
-        mbar_arrive_expect_tx(bar(B_Q_SMEM), kQBlockBytes);
-        tma_load_2d(sbase + q_block_off(8), &q_map, 8 * 64, r * a.H, bar(B_Q_SMEM));
-      }
+    if (lane == 0 && !*abort_flag) {  // Q[r] (128 rows) -> stages 1 and 2 by TMA
+      mbar_arrive_expect_tx(bar(B_Q_SMEM), kCbK * kQBlockBytes);
+      for (int cb = 0; cb < kCbK; ++cb)
+        tma_load_2d(sbase + q_block_off(cb), &q_map, cb * 64, r * a.H, bar(B_Q_SMEM));
     }
     finish();
     return;
@@ -811,8 +805,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (wait_bar_all(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
         tc_fence_after();
         for (int t = 0; t < n_tiles; ++t) {
-          const int s = t % kStages, b = t % kSBufs;
-          const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t / kSBufs) & 1u;
+          const int s = t % kStagesS, b = t % kSBufs;
+          const uint32_t ph = (uint32_t)(t / kStagesS) & 1u, pb = (uint32_t)(t / kSBufs) & 1u;
           if (!wait_bar_all(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
           if (!wait_bar_all(bar(B_S_EMPTY + b), pb ^ 1u, abort_flag, a.error_word)) break;
           tc_fence_after();
@@ -835,12 +829,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t vdesc0 = desc_sw128(sbase + OFF_STAGE, kBlockBytes, 1024);
       uint32_t corr = 0;
       for (int t = 0; t < n_tiles; ++t) {
-        const int s = t % kStages, b = t % kPBufs;
-        const uint32_t ph = (uint32_t)(t / kStages) & 1u, pb = (uint32_t)(t / kPBufs) & 1u;
+        const int s = t % kStagesV, b = t % kPBufs;
+        const uint32_t ph = (uint32_t)(t / kStagesV) & 1u, pb = (uint32_t)(t / kPBufs) & 1u;
         if (lane == 0) mbar_arrive_expect_tx(bar(B_P_FULL + b), kPCopyBytes);
         __syncwarp();
         if (!wait_bar_all(bar(B_KV_FULL + s), ph, abort_flag, a.error_word)) break;
         if (!wait_bar_all(bar(B_P_FULL + b), pb, abort_flag, a.error_word, true)) break;
+        // P arrived by the score CTA's stores (generic proxy): order them before
+        // this thread's MMAs, which read shared memory through the async proxy
+        fence_proxy_async_smem();
         const uint32_t* flags =
             reinterpret_cast<const uint32_t*>(smem + OFF_P + b * kPBufBytes + kPFlagOff);
         if (t > 0 && (flags[0] | flags[4] | flags[8] | flags[12])) {
@@ -888,8 +885,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // of row h sits at chunk position c ^ (h % 8) (conflict-free reads).
     uint32_t qmax = 0;  // bf16 magnitudes seen (FP8 rows: Q must fit fp16)
     bool ok = wait_bar_all(bar(B_Q_SMEM), 0, abort_flag, a.error_word);
-    for (int round = 0; round < 2; ++round) {  // blocks 0..7, then block 8
-      for (int c0 = round ? 256 : 0; ok && c0 < (round ? kD / 2 : 256); c0 += 16) {
+    if (ok) {
+      for (int c0 = 0; c0 < kD / 2; c0 += 16) {
         uint32_t v[16];
         const unsigned char* blk = smem + q_block_off(c0 / 32) + h * 128;
 #pragma unroll
@@ -914,12 +911,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tmem_st16(tm + lane_off + TM_Q + c0, v);
       }
-      if (round == 0) {
-        mbar_arrive(bar(B_Q_HALF));  // blocks 0..7 read: block 8 may overwrite 0..3
-        ok = ok && wait_bar_all(bar(B_Q_SMEM), 1, abort_flag, a.error_word);
-      }
-    }
-    if (ok) {
       tmem_st_wait();
       if (FP8 && ValueLoader::overflow(qmax)) err |= HS_DEV_ERR_VALUE;
     }
@@ -972,7 +963,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // P buffer t % kPBufs is free once the value CTA finished tile t - kPBufs
       if (!wait_bar_all(bar(B_P_EMPTY + pbuf_i), ppar ^ 1u, abort_flag, a.error_word)) break;
-      unsigned char* pbuf = smem + OFF_P + pbuf_i * kPBufBytes;
+      // the value CTA's P buffer and its barrier (cluster addresses)
+      const uint32_t pbuf = peer_p + pbuf_i * kPBufBytes;
+      const uint32_t pbar = peer_pfull + 8u * pbuf_i;
       // p = 2^(scale_log2 * x - m_used); invalid rows give p = 0.  m_used is -inf
       // only while no valid row has been seen, and then every p is 0.
       const float neg_m = -m_used;
@@ -992,21 +985,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         // P [128 heads x 64 rows], K-major core matrices (head group, row group)
         const uint32_t off = (uint32_t)(((h >> 3) * (kTile / 8) + kbg) * 128 + (h & 7) * 16);
-        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        st_async_v4(pbuf + off, make_uint4(pk[0], pk[1], pk[2], pk[3]), pbar);
       }
-      reinterpret_cast<float*>(pbuf + kPAlphaOff)[h] = alpha;
+      st_async_b32(pbuf + kPAlphaOff + 4u * (uint32_t)h, __float_as_uint(alpha), pbar);
       const uint32_t any = __ballot_sync(0xffffffffu, rescale && t > 0);
-      if (lane == 0) reinterpret_cast<uint32_t*>(pbuf + kPFlagOff + 16 * wq)[0] = any;
-      fence_proxy_async_smem();  // generic-proxy writes -> visible to the bulk copies
-      __syncwarp();
-      if (lane == 0) {  // this warp's slice -> the value CTA
-        const uint32_t src = sbase + OFF_P + pbuf_i * kPBufBytes;
-        const uint32_t dst = peer_p + pbuf_i * kPBufBytes;
-        const uint32_t fb = peer_pfull + 8u * pbuf_i;
-        bulk_copy_s2cluster(dst + wq * kPWarpBytes, src + wq * kPWarpBytes, kPWarpBytes, fb);
-        bulk_copy_s2cluster(dst + kPAlphaOff + wq * 128, src + kPAlphaOff + wq * 128, 128, fb);
-        bulk_copy_s2cluster(dst + kPFlagOff + wq * 16, src + kPFlagOff + wq * 16, 16, fb);
-      }
+      if (lane == 0) st_async_v4(pbuf + kPFlagOff + 16u * (uint32_t)wq, make_uint4(any, 0u, 0u, 0u), pbar);
     }
     // final m, l for this head -> value CTA
     st_cluster_f32(mapa(sbase + OFF_ML + 4 * h, 1), m_used);
