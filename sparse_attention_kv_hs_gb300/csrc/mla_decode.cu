@@ -23,8 +23,10 @@
 //     rescale is rare and off the common path) and write the output through
 //     shared memory in coalesced rows.
 // Row loads.  Each CTA loads the tile rows it needs itself, so the two stage
-// rings never wait on each other: CTA 0 gathers the whole 576-column rows by
-// TMA (tile::gather4, 128-byte swizzle, straight into the operand layout);
+// rings never wait on each other: CTA 0's K tiles come by TMA (tile::gather4,
+// 128-byte swizzle, straight into the operand layout) into a 3-stage ring,
+// the rope block from CTA 1's otherwise idle TMA unit (multicast to CTA 0),
+// the rest from CTA 0's own;
 // CTA 1's eight loader warps move the 512 value columns with 16-byte vector
 // loads, converting them to fp16 through registers, with the loads for the
 // next tile issued before the stage frees up.  Pools of FP8 rows (656 bytes:
@@ -70,8 +72,8 @@ constexpr int kStagesS = 3, kStagesV = 2;
 constexpr int kThreads = 512;
 // Warp roles (four warpgroups of four warps):
 //   warp 0       MMA issuer               warp 1 (CTA 0)  Q load
-//   warps 2..3   idle                     warps 4..11     row loaders (CTA 0: TMA
-//                                         gathers; CTA 1: vector loads + fp16)
+//   warp 2 (CTA 1) rope-block gathers      warps 4..11     row loaders (CTA 0: TMA
+//     into CTA 0; other warps 2..3 idle    gathers; CTA 1: vector loads + fp16)
 //   warps 12..15 softmax (CTA 0) / rescale + epilogue (CTA 1)
 constexpr int kLoadWarp0 = 4;
 constexpr int kLoadWarps = 8;
@@ -144,8 +146,17 @@ enum {
   B_MMA_IDLE = 25,   // (CTA 1) commit: earlier P.V MMAs finished
   B_ML_FULL = 26,    // (CTA 1) softmax's final m, l -> epilogue
   B_FINAL = 27,      // MMA issuer's last commit
-  B_COUNT = 28
+  B_XEMPTY = 28,     // [3] (CTA 1) score MMA commit (multicast): a K stage is free for CTA 1's gathers
+  B_XQ = 31,         // (CTA 1) CTA 0's Q has left stages 1-2
+  B_COUNT = 32
 };
+// Column blocks of each bf16 K tile (the last ones: the rope block) that CTA
+// 1's TMA unit gathers into CTA 0's stage.  The loop is bound by CTA 0's TMA
+// gather rate (~23 B/clk); CTA 1's TMA unit is otherwise idle.  One block: 41
+// us per call of 32 x 2048 rows against 44 with none; two or three: 47.6 (CTA
+// 1's own intake becomes the bound).
+constexpr int kXBlocks = 1;
+static_assert(kXBlocks >= 1 && kXBlocks * 16 <= 32, "one warp issues CTA 1's gathers");
 constexpr int kSBufs = 3;  // S accumulators in TMEM (CTA 0)
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 
@@ -259,6 +270,18 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+// The same, multicast: the rows land at the same offset in the shared memory
+// of every CTA in cta_mask, each completing its own barrier at bar's offset.
+__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const CUtensorMap* map, int x, int y0,
+                                               int y1, int y2, int y3, uint32_t bar,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar),
+      "h"(cta_mask)
       : "memory");
 }
 // Register budget of this warpgroup from here on (all four of its warps run
@@ -669,6 +692,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_MMA_IDLE), 1);
     mbar_init(bar(B_ML_FULL), 128);
     mbar_init(bar(B_FINAL), 1);
+    for (int i = 0; i < kStagesS; ++i) mbar_init(bar(B_XEMPTY + i), 1);
+    mbar_init(bar(B_XQ), 1);
     // swizzled TMA destinations and descriptors assume a 1024-byte aligned base
     *abort_flag = (sbase & 1023u) ? 1 : 0;
     if (sbase & 1023u) atomicOr(a.error_word, HS_DEV_ERR_INTERNAL);
@@ -750,10 +775,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     } else if (rank == 0) {
-      // CTA 0: the whole 576-column rows by TMA (written straight into the
-      // swizzled stage, one shared-memory pass).  Lanes 0..15 of the eight
-      // warps issue the 9 x 16 gathers of 4 rows; a row id of -1 reads past the
-      // tensor, which fills zeros.  Tile 1 waits for Q to leave stages 1-2.
+      // CTA 0: the 576-column rows by TMA (written straight into the swizzled
+      // stage, one shared-memory pass).  Lanes 0..15 of the eight warps issue
+      // the (9 - kXBlocks) x 16 gathers of 4 rows (CTA 1 gathers the rest into
+      // this stage); a row id of -1 reads past the tensor, which fills zeros.
+      // Tile 1 waits for Q to leave stages 1-2.
       const int lw = warp - kLoadWarp0;
       if (wait_bar_all(bar(B_RID), 0, abort_flag, a.error_word)) {
         for (int t = 0; t < n_tiles; ++t) {
@@ -770,7 +796,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int y2 = rid[2] >= 0 ? rid[2] : a.rows_in_layer;
             const int y3 = rid[3] >= 0 ? rid[3] : a.rows_in_layer;
             const uint32_t dst = sbase + OFF_STAGE + s * kStageBytes + lane * 512;
-            for (int cb = lw; cb < kCbK; cb += kLoadWarps)
+            for (int cb = lw; cb < kCbK - kXBlocks; cb += kLoadWarps)
               tma_gather4(dst + cb * kBlockBytes, &kv_map, cb * 64, y0, y1, y2, y3,
                           bar(B_KV_FULL + s));
           }
@@ -804,6 +830,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t kdesc0 = desc_sw128(sbase + OFF_STAGE, 16, 1024);
       if (wait_bar_all(bar(B_Q_READY), 0, abort_flag, a.error_word)) {
         tc_fence_after();
+        if (!FP8 && lane == 0) mbar_arrive_remote(mapa(bar(B_XQ), 1));  // CTA 1 may fill stages 1-2
+        __syncwarp();
         for (int t = 0; t < n_tiles; ++t) {
           const int s = t % kStagesS, b = t % kSBufs;
           const uint32_t ph = (uint32_t)(t / kStagesS) & 1u, pb = (uint32_t)(t / kSBufs) & 1u;
@@ -818,6 +846,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                          kd + (uint64_t)((((kk >> 2) * kBlockBytes) + (kk & 3) * 32) >> 4),
                          FP8 ? kIdescS16 : kIdescS, kk > 0);
           mma_commit_elect(bar(B_KV_EMPTY + s));
+          if (!FP8) mma_commit_multicast_elect(bar(B_XEMPTY + s), (uint16_t)(1u << 1));
           mma_commit_elect(bar(B_S_FULL + b));
         }
       }
@@ -1097,6 +1126,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (h < a.H && a.lse) a.lse[(int64_t)r * a.H + h] = lse;
     } else {
       a.ws_lse[((int64_t)r * a.splits + split) * kHeads + h] = lse;
+    }
+    finish();
+    return;
+  } else if (rank == 1 && !FP8 && warp == 2) {
+    // ===== CTA 1, warp 2: the last kXBlocks column blocks of each K tile, gathered into CTA 0 =====
+    // (multicast to CTA 0 alone; each lane 4 rows of one block, completing
+    // CTA 0's KV_FULL barrier, once CTA 0's score MMAs released the stage)
+    regs_set<kRegsWG0>();
+    const int g = lane & 15, cbx = kCbK - kXBlocks + (lane >> 4);
+    const bool issuer = (lane >> 4) < kXBlocks;
+    if (wait_bar_all(bar(B_RID), 0, abort_flag, a.error_word)) {
+      for (int t = 0; t < n_tiles; ++t) {
+        const int s = t % kStagesS;
+        if (t == 1 && !wait_bar_all(bar(B_XQ), 0, abort_flag, a.error_word, true)) break;
+        if (!wait_bar_all(bar(B_XEMPTY + s), ((uint32_t)(t / kStagesS) & 1u) ^ 1u, abort_flag,
+                          a.error_word, true))
+          break;
+        if (issuer) {
+          const int32_t* rid = s_rid + t * kTile + 4 * g;
+          const int y0 = rid[0] >= 0 ? rid[0] : a.rows_in_layer;
+          const int y1 = rid[1] >= 0 ? rid[1] : a.rows_in_layer;
+          const int y2 = rid[2] >= 0 ? rid[2] : a.rows_in_layer;
+          const int y3 = rid[3] >= 0 ? rid[3] : a.rows_in_layer;
+          tma_gather4_mc(sbase + OFF_STAGE + s * kStageBytes + cbx * kBlockBytes + g * 512, &kv_map,
+                         cbx * 64, y0, y1, y2, y3, bar(B_KV_FULL + s), (uint16_t)(1u << 0));
+        }
+        __syncwarp();
+      }
     }
     finish();
     return;
