@@ -391,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     stage_host_rows(hsrc, smem + fp.stage, rv, n_stage, [&](int i) { return f_p[i]; });
     // (2) CTA 0 has written the row id of every miss
     int* s_ok = s_warp + kWarps;
-    if (tid == 0) *s_ok = wait_peer_bar(my_bar, 0) ? 1 : 0;
+    if (tid < 32) {  // the whole warp polls, so that it sees the phase at once
+      const bool got = wait_peer_bar(my_bar, 0);
+      if (tid == 0) *s_ok = got ? 1 : 0;
+    }
     __syncthreads();
     const bool ok = *s_ok != 0;
     if (ok) {
@@ -573,7 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
 
   // ---- 4. serve misses: metadata, row ids, log --------------------------
   if (C > 1) {  // (1) every fetch CTA has read the position -> slot array
-    if (tid == 0) s_warp[kWarps + 1] = wait_peer_bar(my_bar, 0) ? 1 : 0;
+    if (tid < 32) {  // the whole warp polls, so that it sees the phase at once
+      const bool got = wait_peer_bar(my_bar, 0);
+      if (tid == 0) s_warp[kWarps + 1] = got ? 1 : 0;
+    }
     __syncthreads();
     if (!s_warp[kWarps + 1]) {  // never updated under a reader: serve nothing
       err |= HS_DEV_ERR_WAIT;
