@@ -312,6 +312,25 @@ def measure_d2h_peak(torch, nbytes=1 << 30, reps=10):
     return best
 
 
+def pretouch_host_pool(torch, hs, pool, chunk=1 << 30):
+    """Setup, before the warm-up: the GPU reads the whole host pool once (its
+    device alias, 1 GiB at a time).  On some boxes the GPU's first read of each
+    host page is slow (the step-0 fill took 13-17 ms against ~1 ms on others,
+    and the following steps ran ~10x slower until the pages had been seen);
+    this keeps that one-time cost out of the warm-up and the timed steps.
+    Returns the time taken (ms)."""
+    total = int(pool.raw.host_pool_bytes) // 16 * 16
+    scratch = torch.empty(min(chunk, total), dtype=torch.uint8, device="cuda")
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for off in range(0, total, chunk):
+        hs.hs_host_read(int(pool.raw.host_pool_device) + off, min(chunk, total - off), scratch)
+    b.record()
+    b.synchronize()
+    del scratch
+    return a.elapsed_time(b)
+
+
 def measure_host_read_peak(torch, hs, pool, nbytes=1 << 30, reps=10):
     """Kernel reads of mapped pinned host memory -> device (GB/s), best of reps.
     Reads the pool's own host pool through the device alias libhs returns."""
@@ -534,6 +553,7 @@ def run_ours(args):
         pad = torch.full((R * K,), -1, dtype=torch.int32, device=dev)
         if lib.hs_gather(ph, 0, pad.data_ptr(), R * K, gather_d.data_ptr(), sptr) != 0:
             raise RuntimeError("pre-load gather failed")
+    pretouch_ms = pretouch_host_pool(torch, hs, pool)
     torch.cuda.synchronize()
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     c0.record(stream)
@@ -648,6 +668,7 @@ def run_ours(args):
             "miss_rows_per_step": misses_main / args.steps,
             "cold_step": {"ms": cold_ms, "miss_rows": cold_misses,
                           "note": "step 0 (empty hot buffers), before the warm-up; not in value"},
+            "host_pool_pretouch_ms": pretouch_ms,
             "schedule": ("hs_decode_step: the later layers' RESOLVE on a copy stream "
                          + ("after layer 0's RESOLVE, beside its attention" if fp8 else
                             "beside layer 0's RESOLVE")
@@ -826,6 +847,7 @@ def run_mixed(args):
     app_index = {(t, r, page): i for i, (t, r, page, blk) in enumerate(app)}
     h2d_peak = measure_h2d_peak(torch) if not args.profile else float("nan")
     d2h_peak = measure_d2h_peak(torch) if not args.profile else float("nan")
+    pretouch_ms = pretouch_host_pool(torch, hs, pool)
     for t in range(args.warmup):
         one_step(t)
     torch.cuda.synchronize()
@@ -878,6 +900,7 @@ def run_mixed(args):
         line = {
             "metric": METRIC, "value": weak_scaling_rate(R * K * L, args.steps, world, elapsed_ms),
             "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "host_pool_pretouch_ms": pretouch_ms,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8-e4m3 rows (moved as bytes)" if fp8 else "bf16",
             "data": "synthetic (seeded generator; no dataset)",
@@ -983,6 +1006,7 @@ def run_spec(args):
 
     peaks = load_peaks()
     h2d_peak = measure_h2d_peak(torch) if not args.profile else float("nan")
+    pretouch_ms = pretouch_host_pool(torch, hs, pool)
     for t in range(args.warmup):
         fused_step(t)
     torch.cuda.synchronize()
@@ -1035,6 +1059,7 @@ def run_spec(args):
         line = {
             "metric": METRIC, "value": weak_scaling_rate(R * L * T * K, args.steps, world, elapsed_ms),
             "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "host_pool_pretouch_ms": pretouch_ms,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8-e4m3 rows, fp16 MMA operands" if fp8 else "bf16",
             "data": "synthetic (seeded generator; no dataset)",
