@@ -193,6 +193,25 @@ class ClockSampler:
         self.proc = None
         self.path = None
 
+    def _lines(self):
+        try:
+            with open(self.path) as f:
+                return sum(1 for line in f if line.count(",") >= 8)
+        except OSError:
+            return 0
+
+    def wait_ready(self, timeout_s=20.0):
+        """Return once nvidia-smi writes samples: its start-up can take a second
+        or more, and while it initialises the CUDA launches of the first timed
+        steps ran up to ~10x slower.  A timed region of a few milliseconds holds
+        no 100-ms sample of its own, so the record keeps the samples from here
+        on (the GPU has just run the warm-up) together with those taken during
+        the timed region."""
+        t0 = time.time()
+        while self.proc is not None and self._lines() < 2 and time.time() - t0 < timeout_s:
+            time.sleep(0.05)
+        time.sleep(0.2)
+
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
@@ -312,22 +331,18 @@ def measure_d2h_peak(torch, nbytes=1 << 30, reps=10):
     return best
 
 
-def pretouch_host_pool(torch, hs, pool, chunk=1 << 30):
-    """Setup, before the warm-up: the GPU reads the whole host pool once (its
-    device alias, 1 GiB at a time).  On some boxes the GPU's first read of each
-    host page is slow (the step-0 fill took 13-17 ms against ~1 ms on others,
-    and the following steps ran ~10x slower until the pages had been seen);
-    this keeps that one-time cost out of the warm-up and the timed steps.
-    Returns the time taken (ms)."""
-    total = int(pool.raw.host_pool_bytes) // 16 * 16
-    scratch = torch.empty(min(chunk, total), dtype=torch.uint8, device="cuda")
+def pretouch_host_pool(torch, hs, pool):
+    """Setup, before the warm-up: the GPU reads the whole host pool once
+    (hs_pool_touch_host).  On some boxes the GPU's first read of each host page
+    is slow (the step-0 fill took 13-17 ms against ~1 ms on others, and the
+    following steps ran ~10x slower until the pages had been seen); this keeps
+    that one-time cost out of the warm-up and the timed steps.  Returns the
+    time taken (ms)."""
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    for off in range(0, total, chunk):
-        hs.hs_host_read(int(pool.raw.host_pool_device) + off, min(chunk, total - off), scratch)
+    hs.hs_pool_touch_host(pool.handle)
     b.record()
     b.synchronize()
-    del scratch
     return a.elapsed_time(b)
 
 
@@ -569,7 +584,7 @@ def run_ours(args):
     clocks = ClockSampler(local) if not args.profile else None
     if clocks:
         clocks.start()
-        time.sleep(0.3)
+        clocks.wait_ready()
     # sequential steps timed launch by launch: the main region itself for the
     # gather / resolve workloads, a second pass after it for the attention one
     n_ev = args.steps if not attention else kern_steps
@@ -856,7 +871,7 @@ def run_mixed(args):
     clocks = ClockSampler(local) if not args.profile else None
     if clocks:
         clocks.start()
-        time.sleep(0.3)
+        clocks.wait_ready()
     evr = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     launches[0] = 0
     off_steps = [t for t in range(args.warmup, steps_total) if scen.appends[t]]
@@ -1015,7 +1030,7 @@ def run_spec(args):
     clocks = ClockSampler(local) if not args.profile else None
     if clocks:
         clocks.start()
-        time.sleep(0.3)
+        clocks.wait_ready()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t_start.record(stream)

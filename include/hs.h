@@ -428,6 +428,15 @@ hs_status hs_wait_offload(void* done_event, int64_t timeout_ns);
  * null or misaligned pointers. */
 hs_status hs_host_read(const void* host_device_ptr, int64_t bytes, void* dst, void* stream);
 
+/* Have the GPU read the pool's whole host pool once (through its device
+ * alias; the data is discarded).  On some machines the GPU's first read of
+ * each host page is slow (a decode step's misses then took ~10x longer until
+ * the pages had been read once), so a server calls this once after creating
+ * the pool, before serving.  Reads p->host_bytes at the host link's rate (about
+ * 23 ms for 4.8 GB at 211 GB/s); changes nothing.  Async on `stream`.
+ * HS_ERR_INVALID for a NULL pool. */
+hs_status hs_pool_touch_host(hs_pool* pool, void* stream);
+
 /* Self-test of the in-kernel bounded waits that keep a stalled hand-off from
  * hanging the GPU: two one-thread kernels each wait on an mbarrier of their
  * own CTA that nothing arrives on, with the waits the attention kernel and

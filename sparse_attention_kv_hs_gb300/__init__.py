@@ -46,7 +46,7 @@ EXPORTED = (
     "hs_sparse_mla_decode_noalloc", "hs_decode_step", "hs_decode_step_tokens", "hs_resolve_tokens",
     "hs_selftest_bounded_waits",
     "hs_sparse_mla_decode_tokens", "hs_noalloc_check_errors", "hs_wait_offload",
-    "hs_pool_host_numa_node",
+    "hs_pool_host_numa_node", "hs_pool_touch_host",
 )
 
 
@@ -119,6 +119,7 @@ def load(build: bool = True) -> ctypes.CDLL:
         "hs_noalloc_check_errors": [ctypes.POINTER(i32)],
         "hs_wait_offload": [p, i64],
         "hs_pool_host_numa_node": [p, ctypes.POINTER(i32)],
+        "hs_pool_touch_host": [p, p],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -327,6 +328,10 @@ def hs_wait_offload(done_event, timeout_ns: int) -> int:
     if st not in (HS_OK, HS_ERR_TIMEOUT):
         raise HsError(st, "hs_wait_offload")
     return st
+
+
+def hs_pool_touch_host(pool: int, stream=None) -> None:
+    _check(load().hs_pool_touch_host(pool, _stream(stream)), "hs_pool_touch_host")
 
 
 def hs_pool_host_numa_node(pool: int) -> int:

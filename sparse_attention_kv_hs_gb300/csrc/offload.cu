@@ -75,6 +75,19 @@ __global__ void __launch_bounds__(512) host_read_kernel(const uint4* __restrict_
   for (; i < n; i += stride) dst[i] = __ldcs(src + i);
 }
 
+// Reads every 16-byte vector of the n at src and discards it, so that the
+// GPU has read each host page once (volatile loads: none may be dropped).
+__global__ void __launch_bounds__(512) touch_host_kernel(const uint4* __restrict__ src, int64_t n) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+    uint32_t a, b, c, d;
+    asm volatile("ld.volatile.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
+                 : "l"(src + i));
+    asm volatile("" ::"r"(a), "r"(b), "r"(c), "r"(d));
+  }
+}
+
 }  // namespace
 
 extern "C" hs_status hs_offload_pages(hs_pool* p, int32_t num_pages, const int32_t* reqs,
@@ -138,6 +151,19 @@ extern "C" hs_status hs_host_read(const void* host_device_ptr, int64_t bytes, vo
   HS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   host_read_kernel<<<sms * 4, 512, 0, hs_stream(stream)>>>(
       static_cast<const uint4*>(host_device_ptr), bytes / 16, static_cast<uint4*>(dst));
+  HS_CUDA_TRY(cudaGetLastError());
+  return HS_OK;
+}
+
+extern "C" hs_status hs_pool_touch_host(hs_pool* p, void* stream) {
+  if (!p || !p->host_pool_dev) return HS_ERR_INVALID;
+  int dev = 0, sms = 0;
+  HS_CUDA_TRY(cudaGetDevice(&dev));
+  HS_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t n = (int64_t)(p->host_bytes / 16);
+  if (n == 0) return HS_OK;
+  touch_host_kernel<<<sms * 4, 512, 0, hs_stream(stream)>>>(
+      static_cast<const uint4*>(p->host_pool_dev), n);
   HS_CUDA_TRY(cudaGetLastError());
   return HS_OK;
 }

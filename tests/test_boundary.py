@@ -102,3 +102,4 @@ def test_wait_offload_argument_errors_need_no_gpu():
     lib = hs.load()
     assert lib.hs_wait_offload(None, 1000) == hs.HS_ERR_INVALID
     assert lib.hs_wait_offload(ctypes.c_void_p(8), -1) == hs.HS_ERR_INVALID
+    assert lib.hs_pool_touch_host(None, None) == hs.HS_ERR_INVALID
