@@ -212,10 +212,13 @@ hs_status hs_resolve(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
  *   miss_count   device int32 [num_layers][R] or NULL: misses served
  *   miss_log     device int32 [num_layers][R][T*K][3] or NULL: (j, position,
  *                slot) per served miss, j indexing the unit's T*K list
- * Size limit: at most 8192 entries (T*K) per unit, and the unit's tables for
- * them and B slots must fit one CTA's shared memory (T = 4 at K = 2048 with
- * B up to 12288, when the page table has at most 4096 pages); otherwise
- * HS_ERR_INVALID.  Async, graph-capturable, no allocation. */
+ * Sizes: B at most 16384 slots.  A list whose tables fit one CTA's shared
+ * memory (at most 8192 entries, e.g. T = 4 at K = 2048 with B up to 12288)
+ * runs as one launch; a longer one as launches over groups of its tokens, in
+ * order, after one pass that pins every hit of the whole list, with the same
+ * row ids, slot state and miss log as one launch over the list.  HS_ERR_INVALID
+ * if B is larger or even one token's tables do not fit.  Async,
+ * graph-capturable, no allocation. */
 hs_status hs_resolve_tokens(hs_pool* pool, int32_t layer_begin, int32_t num_layers,
                             int32_t num_tokens, const int32_t* topk_idx,
                             const int32_t* d_step, int32_t* out_row_ids,

@@ -31,6 +31,7 @@ struct hs_pool {
   int32_t* inv;         // [L][host_tokens]: hot slot holding each host row, or -1
   int32_t* step;        // scalar
   int32_t* error_word;  // scalar
+  int32_t* resolve_counts;  // [L][R]: running miss counts of a list resolved in token groups
 
   // sparse MLA decode workspace (split-K partials)
   uint16_t* attn_o;  // [R][max_splits][128][512] fp16 partials

@@ -93,6 +93,7 @@ void free_pool(hs_pool* p) {
   cudaFree(p->inv);
   cudaFree(p->step);
   cudaFree(p->error_word);
+  cudaFree(p->resolve_counts);
   hs_attn_workspace_free(p);
   if (p->order_event) cudaEventDestroy(p->order_event);
   if (p->step_events) {
@@ -256,6 +257,7 @@ extern "C" hs_status hs_pool_create(const hs_pool_desc* desc, hs_pool** out) {
   }
   if ((st = dev_alloc(&p->step, 1)) != HS_OK) goto fail;
   if ((st = dev_alloc(&p->error_word, 1)) != HS_OK) goto fail;
+  if ((st = dev_alloc(&p->resolve_counts, (size_t)L * R)) != HS_OK) goto fail;
   if ((st = hs_attn_workspace_init(p)) != HS_OK) goto fail;
   if (cudaEventCreateWithFlags(&p->order_event, cudaEventDisableTiming) != cudaSuccess) {
     p->order_event = nullptr;

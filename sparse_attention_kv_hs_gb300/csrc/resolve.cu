@@ -66,6 +66,13 @@ struct ResolveArgs {
   int32_t sel_bits, kpt, bpt;
   int32_t copy_ctas;  // C: CTAs (a cluster) per unit
   int32_t smem_bytes; // dynamic shared memory per CTA (tables + staging)
+  // A list longer than one CTA's tables runs as several launches over groups
+  // of its tokens: this launch's K entries start at entry j_base of each
+  // unit's list of list_stride entries; with `accumulate`, miss_count already
+  // holds the earlier groups' misses (their log entries come first) and this
+  // launch adds its own.
+  int64_t list_stride;
+  int32_t j_base, accumulate;
 };
 
 // Both layouts start with one mbarrier at offset 0, so each CTA of a cluster
@@ -310,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   const int64_t call_unit = (int64_t)li * a.R + r;
   const int K = a.K, B = a.B, P = P_CT ? P_CT : a.P;
   const int rv = RV_CT ? RV_CT : a.row_vec;
-  const int32_t* topk = a.topk + call_unit * K;
-  int32_t* out = a.out_rows + call_unit * K;
+  const int32_t* topk = a.topk + call_unit * a.list_stride + a.j_base;
+  int32_t* out = a.out_rows + call_unit * a.list_stride + a.j_base;
   const int32_t* ptab = a.page_table + (int64_t)r * a.max_pages;
   int32_t* inv_u = a.inv + (int64_t)l * a.host_tokens + a.host_off[r];
   const uint4* hsrc = a.host_pool + ((int64_t)l * a.host_tokens + a.host_off[r]) * rv;
@@ -430,13 +437,19 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
   int32_t* g_stamp = a.slot_stamp + unit * B;
   int32_t* g_order = a.lru_order + unit * B;
   const int32_t step = *a.d_step;
+  // earlier token groups' misses come first in the log and the count (read
+  // here, before the block barriers that precede this launch's own count)
+  const int32_t log_base = a.accumulate ? __ldcg(a.miss_count + call_unit) : 0;
 
   int err = 0;
   if (tid == 0) *s_err = 0;
   // ---- 0. load unit state, clear tables ---------------------------------
+  // a slot already stamped with this step (a hit of a later token group, or a
+  // slot an earlier group used) counts as used: it is no victim, and it moves
+  // to the back of the order with this launch's hits and refills
   for (int s = tid; s < B; s += kThreads) {
     s_order[s] = g_order[s];
-    s_flag[s] = 0;
+    s_flag[s] = g_stamp[s] == step ? 1 : 0;
   }
   for (int h = tid; h <= sel_mask; h += kThreads) s_sel[h] = -1;
   for (int i = tid; i < hot_per_req; i += kThreads)
@@ -586,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       n_serve = 0;
     }
   }
-  int32_t* log = a.miss_log ? a.miss_log + call_unit * (int64_t)K * 3 : nullptr;
+  int32_t* log = a.miss_log ? a.miss_log + (call_unit * a.list_stride + log_base) * 3 : nullptr;
   for (int i = tid; i < n_miss_total; i += kThreads) {
     const int j = s_miss_j[i];
     if (i < n_serve) {
@@ -598,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       g_stamp[s] = step;
       out[j] = s_hot[s / P] * P + s % P;
       if (log) {
-        log[3 * i + 0] = j;
+        log[3 * i + 0] = a.j_base + j;
         log[3 * i + 1] = p;
         log[3 * i + 2] = s;
       }
@@ -606,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
       out[j] = -1;
     }
   }
-  if (tid == 0 && a.miss_count) a.miss_count[call_unit] = n_serve;
+  if (tid == 0 && a.miss_count) a.miss_count[call_unit] = log_base + n_serve;
   if (err) atomicOr(s_err, err);
   __syncthreads();
   if (tid == 0 && *s_err) atomicOr(a.error_word, *s_err);
@@ -706,6 +719,25 @@ hs_status hs_resolve_configure(int K, int B, int P, int max_pages, size_t* smem_
 
 namespace {
 
+// Before a list runs as several token groups: every hot hit of the whole list
+// gets this step's stamp, so that no group takes another group's hit as a
+// victim (the groups then resolve exactly as one launch over the whole list).
+__global__ void __launch_bounds__(kThreads) protect_hits_kernel(const ResolveArgs a,
+                                                                int32_t list_len) {
+  const int r = blockIdx.x, li = blockIdx.y, l = a.layer_begin + li;
+  const int64_t unit = (int64_t)l * a.R + r, call_unit = (int64_t)li * a.R + r;
+  const int32_t* topk = a.topk + call_unit * a.list_stride;
+  const int32_t* inv_u = a.inv + (int64_t)l * a.host_tokens + a.host_off[r];
+  int32_t* g_stamp = a.slot_stamp + unit * a.B;
+  const int32_t ctx = a.ctx_len[r], step = *a.d_step;
+  for (int j = threadIdx.x; j < list_len; j += kThreads) {
+    const int32_t p = topk[j];
+    if (p < 0 || p >= ctx) continue;
+    const int32_t slot = inv_u[p];
+    if (slot >= 0) g_stamp[slot] = step;
+  }
+}
+
 // RESOLVE of `num_tokens` verify tokens per unit (1 outside speculative
 // decoding): the unit's list is their num_tokens * K entries, token after token.
 hs_status launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers, int32_t num_tokens,
@@ -734,22 +766,36 @@ hs_status launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers, in
   a.layer_begin = layer_begin;
   a.R = p->d.num_requests;
   a.ktok = p->d.top_k;
-  a.K = num_tokens * p->d.top_k;
   a.B = p->d.hot_slots;
   a.P = p->d.page_tokens;
   a.max_pages = p->d.max_pages;
   a.row_vec = (int32_t)(hs_row_bytes(p->d) / 16);
-  a.sel_bits = ceil_log2(2 * (int64_t)a.K) < 5 ? 5 : ceil_log2(2 * (int64_t)a.K);
-  a.kpt = (a.K + kThreads - 1) / kThreads;
   a.bpt = (a.B + kThreads - 1) / kThreads;
-  if (a.kpt > 8 || a.bpt > 16) return HS_ERR_INVALID;
+  if (a.bpt > 16) return HS_ERR_INVALID;
   // The kernel's dynamic shared-memory limit was raised by hs_pool_create
   // (hs_resolve_configure): nothing here may call outside the stream.
   const size_t smem = p->resolve_smem;
   const int ptab_pages = a.max_pages <= kMaxSmemPages ? a.max_pages : 0;
-  if (num_tokens > 1 && (smem_plan(a.K, a.B, a.P, a.sel_bits, ptab_pages).total > smem ||
-                         fetch_plan(a.K, a.sel_bits).stage > smem))
-    return HS_ERR_INVALID;  // the list's tables do not fit one CTA's shared memory
+  // Tokens per launch: all of them when their list's tables fit one CTA (at
+  // most 8 entries per thread, the tables and fetch lists in shared memory);
+  // otherwise groups of the most tokens that fit, in token order.
+  auto set_list = [&](int tokens) {
+    a.K = tokens * a.ktok;
+    a.sel_bits = ceil_log2(2 * (int64_t)a.K) < 5 ? 5 : ceil_log2(2 * (int64_t)a.K);
+    a.kpt = (a.K + kThreads - 1) / kThreads;
+  };
+  auto fits = [&](int tokens) {
+    set_list(tokens);
+    if (a.kpt > 8) return false;
+    return tokens == 1 || (smem_plan(a.K, a.B, a.P, a.sel_bits, ptab_pages).total <= smem &&
+                           fetch_plan(a.K, a.sel_bits).stage <= smem);
+  };
+  int group = num_tokens;
+  while (group >= 1 && !fits(group)) --group;
+  if (group < 1) return HS_ERR_INVALID;
+  a.list_stride = (int64_t)num_tokens * a.ktok;
+  a.j_base = 0;
+  a.accumulate = 0;
   a.smem_bytes = (int32_t)smem;
   // CTAs per unit: the largest cluster size (8, 4, 2) whose clusters, one per
   // unit, all run at once; else one CTA per unit
@@ -774,12 +820,29 @@ hs_status launch_resolve(hs_pool* p, int32_t layer_begin, int32_t num_layers, in
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = C > 1 ? 1 : 0;
-  if (a.P == 256 && a.row_vec == 72)  // bf16 [576] rows
-    HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<256, 72>, a));
-  else if (a.P == 256 && a.row_vec == 41)  // FP8 rows (656 bytes)
-    HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<256, 41>, a));
-  else
-    HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<0, 0>, a));
+  auto launch = [&]() -> hs_status {
+    if (a.P == 256 && a.row_vec == 72)  // bf16 [576] rows
+      HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<256, 72>, a));
+    else if (a.P == 256 && a.row_vec == 41)  // FP8 rows (656 bytes)
+      HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<256, 41>, a));
+    else
+      HS_CUDA_TRY(cudaLaunchKernelEx(&cfg, resolve_kernel<0, 0>, a));
+    return HS_OK;
+  };
+  if (group == num_tokens) return launch();
+  // Token groups, in order, after every hit of the whole list is stamped; the
+  // miss count (the pool's scratch when the caller passes none) carries each
+  // group's log offset to the next.
+  if (!a.miss_count) a.miss_count = p->resolve_counts + (int64_t)layer_begin * a.R;
+  protect_hits_kernel<<<dim3(a.R, num_layers), kThreads, 0, stream>>>(a, (int32_t)a.list_stride);
+  HS_CUDA_TRY(cudaGetLastError());
+  for (int t0 = 0; t0 < num_tokens; t0 += group) {
+    set_list(num_tokens - t0 < group ? num_tokens - t0 : group);
+    a.j_base = t0 * a.ktok;
+    a.accumulate = t0 > 0 ? 1 : 0;
+    const hs_status st = launch();
+    if (st != HS_OK) return st;
+  }
   return HS_OK;
 }
 

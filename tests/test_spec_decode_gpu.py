@@ -28,7 +28,7 @@ def _check(got, ref, what=""):
     assert max_abs <= MAX_ABS and mean_rel <= MEAN_REL, (what, max_abs, mean_rel)
 
 
-def replay_tokens(w, attn_steps=(), attn_requests=None, kv_format=0):
+def replay_tokens(w, attn_steps=(), attn_requests=None, kv_format=0, check_state=False):
     scen = W.Scenario.build(w)
     pool = harness.make_pool(w, scen, kv_format)
     o = harness.make_oracle(w, scen)
@@ -55,6 +55,10 @@ def replay_tokens(w, attn_steps=(), attn_requests=None, kv_format=0):
                 np.testing.assert_array_equal(rows[r], ref_rows, err_msg=f"t={t} l={l} r={r}")
                 assert cnt[r] == len(ref_log), (t, l, r)
                 np.testing.assert_array_equal(log[r, :cnt[r]], ref_log)
+                if check_state:  # every slot's position and stamp
+                    ref_pos, ref_stamp = o.unit_state(l, r)
+                    np.testing.assert_array_equal(pool.slot_pos[l, r].cpu().numpy(), ref_pos)
+                    np.testing.assert_array_equal(pool.slot_stamp[l, r].cpu().numpy(), ref_stamp)
             if t in attn_steps:
                 q = np.stack([np.stack([synth.q(w.seed, r, l, t * T + k, H) for k in range(T)])
                               for r in range(R)])
@@ -145,16 +149,32 @@ def test_repeats_within_and_across_tokens():
     pool.close()
 
 
-def test_lists_too_large_for_one_cta_are_rejected():
-    """T = 5 tokens of K 2048 (10,240 entries, more than one CTA's 8,192) and
-    T = 4 with B = 12,800 (the tables of 8,192 entries exceed one CTA's shared
-    memory; B = 12,288 fits)."""
-    for T, B in ((5, 7 * 2048), (4, 50 * 256)):
-        pool = hs.Pool(1, 1, 2048, B, 256, W.ROW_ELEMS, 256, 65536, 1)
-        t = torch.zeros((1, T, 2048), dtype=torch.int32, device="cuda")
-        with pytest.raises(hs.HsError):
-            hs.hs_resolve_tokens(pool.handle, 0, 1, T, t, pool.step, t.clone())
-        pool.close()
+def test_five_verify_tokens_in_token_groups():
+    """T = 5 tokens of K 2048 (10,240 entries, more than one CTA's 8,192), B =
+    7 K: resolved as token groups (the tables of 4 tokens with B = 14,336 do
+    not fit one CTA) after the pass that pins the whole list's hits; rows,
+    miss counts and logs bit-exact against the oracle every step."""
+    w = W.make("spec", R=4, steps=5, tokens=5)
+    replay_tokens(w, attn_steps={0, 4}, attn_requests={0, 3}, check_state=True)
+
+
+def test_six_verify_tokens_in_token_groups_with_the_largest_hot_buffer():
+    """T = 6 (12,288 entries), B = 8 K = 16,384 slots, the most a unit takes."""
+    w = W.make("spec", R=2, steps=4, tokens=6)
+    replay_tokens(w, check_state=True)
+
+
+def test_five_verify_tokens_through_the_decode_step():
+    """T = 5 through hs_decode_step_tokens (later layers' RESOLVE on the copy stream)."""
+    w = W.make("spec", R=4, steps=3, tokens=5)
+    replay_step_tokens(w, check_steps={2}, attn_requests={0, 3})
+
+
+def test_hot_buffers_above_16384_slots_are_rejected():
+    """T = 7 at K 2048 needs B = 9 K = 18,432 slots: more than a unit takes
+    (the pool refuses it)."""
+    with pytest.raises(hs.HsError):
+        hs.Pool(1, 1, 2048, 9 * 2048, 256, W.ROW_ELEMS, 256, 65536, 1)
 
 
 def test_four_verify_tokens_scaled_down():
