@@ -246,7 +246,9 @@ hs_status hs_gather(hs_pool* pool, int32_t layer, const int32_t* row_ids,
  * magnitude below 65536 exactly (values below 2^-14 lose low bits, at most
  * 2^-25 each) and gives the probabilities 11 significant bits; a value
  * element that is not finite or has magnitude >= 65536 sets error bit VALUE
- * (that request's output is then not meaningful).
+ * (that request's output is then not meaningful).  When K is split between
+ * several CTA pairs, each pair's normalised partial output is held in fp16
+ * (one more rounding, 2^-12 relative) until the bf16 combination.
  * FP8 pools (HS_KV_FP8): both products run on fp16 operands.  q is rounded
  * from bf16 to fp16; a latent value is E4M3(code) * scale formed as fp16 --
  * from the scale rounded to fp16 when every group scale of the 8 rows a
