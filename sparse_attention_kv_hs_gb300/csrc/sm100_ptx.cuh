@@ -2,7 +2,8 @@
 // features the attention kernel uses: mbarriers (with bounded waits),
 // tensor memory (tcgen05.alloc / ld / st), tcgen05.mma with fp32
 // accumulation in TMEM, shared-memory matrix descriptors, and cluster
-// shared memory (remote arrivals, bulk copies between the CTAs of a cluster).
+// shared memory (remote arrivals, remote st.async stores that count their
+// bytes on the receiving CTA's mbarrier).
 #pragma once
 
 #include <cuda_runtime.h>
