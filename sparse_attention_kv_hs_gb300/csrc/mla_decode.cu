@@ -16,12 +16,14 @@
 //     (M=128, N=64, K=576) over 64-row tiles goes to one of three TMEM
 //     accumulators; 4 warps run the online softmax (one thread per head) and
 //     write P in fp16 (11 significant bits; bf16 P would cost ~1.5e-3 relative
-//     error), which per-warp bulk copies send into CTA 1's P ring.
+//     error) straight into CTA 1's P ring by remote st.async stores, which
+//     count their bytes on that buffer's mbarrier in CTA 1.
 //   CTA 1 ("value"): accumulates O += P V (M=128, N=256 x 2, V as an MN-major
-//     operand) with V in fp16 as well.  Its 4 epilogue warps rescale O when the
+//     operand) with V in fp16 as well.  Its 4 rescale warps rescale O when the
 //     running max moved (lazily: only when it grew by more than 2^8, so the
-//     rescale is rare and off the common path) and write the output through
-//     shared memory in coalesced rows.
+//     rescale is rare and off the common path).  After the last tile they and
+//     the 8 loader warps (three warps per TMEM lane quarter) write the output
+//     through shared memory in coalesced rows.
 // Row loads.  Each CTA loads the tile rows it needs itself, so the two stage
 // rings never wait on each other: CTA 0's K tiles come by TMA (tile::gather4,
 // 128-byte swizzle, straight into the operand layout) into a 3-stage ring,
@@ -74,7 +76,8 @@ constexpr int kThreads = 512;
 //   warp 0       MMA issuer               warp 1 (CTA 0)  Q load
 //   warp 2 (CTA 1) rope-block gathers      warps 4..11     row loaders (CTA 0: TMA
 //     into CTA 0; other warps 2..3 idle    gathers; CTA 1: vector loads + fp16)
-//   warps 12..15 softmax (CTA 0) / rescale + epilogue (CTA 1)
+//   warps 12..15 softmax (CTA 0) / rescale + epilogue (CTA 1; the loader
+//     warps join the epilogue)
 constexpr int kLoadWarp0 = 4;
 constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = kLoadWarps * 32;
@@ -127,8 +130,8 @@ __host__ __device__ constexpr uint32_t q_block_off(int cb) {
   return OFF_STAGE + kStageBytes + (uint32_t)cb * kQBlockBytes;
 }
 static_assert(q_block_off(0) % 1024 == 0 && kQBlockBytes % 1024 == 0, "swizzled Q blocks");
-// epilogue staging (4 warps x 8 KiB) reuses the stage region once the last tile is consumed
-static_assert(4 * 8192 <= kStagesV * kStageBytes, "epilogue staging");
+// epilogue staging (12 warps x 8 KiB) reuses the stage region once the last tile is consumed
+static_assert(12 * 8192 <= kStagesV * kStageBytes, "epilogue staging");
 
 // barrier indices (8 bytes each at OFF_BAR)
 enum {
@@ -728,6 +731,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync();
   };
 
+  // Value CTA epilogue: O / l to global memory.  Three warps per TMEM lane
+  // quarter share the 512 columns once the last P.V is done: part 0 (loader
+  // warps 4..7) columns 0..191, part 1 (loader warps 8..11) 192..351, part 2
+  // (the rescale warps 12..15, which also write lse) 352..511.
+  auto epilogue = [&](int part) {
+    const int wq = warp & 3;
+    const int h = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const int c_begin = part == 0 ? 0 : part == 1 ? 192 : 352;
+    const int c_end = part == 0 ? 192 : part == 1 ? 352 : kDV;
+    // 32 columns at a time, through this warp's 8 KiB of the (now idle) stage
+    // region so that the global stores are whole 64-byte runs of a head's row
+    bool ok = wait_bar_all(bar(B_FINAL), 0, abort_flag, a.error_word) && n_tiles > 0;
+    const bool have_ml = wait_bar_all(bar(B_ML_FULL), 0, abort_flag, a.error_word, true);
+    ok = ok && have_ml;  // warp-uniform: gates the warp-collective TMEM loads below
+    tc_fence_after();
+    const float m = have_ml ? reinterpret_cast<const float*>(smem + OFF_ML)[h] : -INFINITY;
+    const float l = have_ml ? reinterpret_cast<const float*>(smem + OFF_ML + 512)[h] : 0.f;
+    const bool has_rows = ok && l > 0.f;  // per head (lane)
+    const float inv_l = has_rows ? 1.f / l : 0.f;
+    const float lse = has_rows ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    const uint32_t stg = sbase + OFF_STAGE + (uint32_t)(warp - kLoadWarp0) * 8192u;
+    // One split: the bf16 output.  Several: this split's partial O / l in fp16
+    // (|O / l| is at most the largest |value|, which the loaders hold below
+    // 65536, so fp16 keeps it; 11 significant bits, against bf16's 8 in the
+    // final output) for the merge kernel.  Both are 16-bit: 64 B per head per
+    // 32 columns.
+    const bool partial = a.splits > 1;
+    uint16_t* dst = partial ? a.ws_o + (((int64_t)r * a.splits + split) * kHeads + wq * 32) * kDV
+                            : a.out + ((int64_t)r * a.H + wq * 32) * kDV;
+    for (int c0 = c_begin; c0 < c_end; c0 += 32) {  // 32 columns at a time (few live registers)
+      uint32_t u[32];
+      if (ok) {
+        const uint32_t oa = tm + lane_off + TM_O + c0;
+        tmem_ld16p(oa, u);
+        tmem_ld16p(oa + 16, u + 16);
+        tmem_ld_wait();
+      }
+      // a head's 32 columns are 4 chunks of 16 B, chunk k at k ^ (lane % 4)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float x = __uint_as_float(u[8 * k + 2 * i]) * inv_l;
+          const float y = __uint_as_float(u[8 * k + 2 * i + 1]) * inv_l;
+          pk[i] = !has_rows ? 0u : partial ? pack_f16x2(x, y) : pack_bf16x2(x, y);
+        }
+        st_shared_v4(stg + lane * 64 + ((k ^ (lane & 3)) << 4),
+                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
+      }
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {  // 8 heads x 64 B per instruction
+        const int row = 8 * i + (lane >> 2), k = lane & 3;
+        const uint4 v = ld_shared_v4(stg + row * 64 + ((k ^ (row & 3)) << 4));
+        if (wq * 32 + row < a.H)
+          *reinterpret_cast<uint4*>(dst + (int64_t)row * kDV + c0 + 8 * k) = v;
+      }
+      __syncwarp();
+    }
+    if (part == 2) {  // lse, one per head
+      if (a.splits == 1) {
+        if (h < a.H && a.lse) a.lse[(int64_t)r * a.H + h] = lse;
+      } else {
+        a.ws_lse[((int64_t)r * a.splits + split) * kHeads + h] = lse;
+      }
+    }
+  };
+
   // Each role first sets its warpgroup's register budget (kRegsWG0 ...); the
   // four warps of a warpgroup always take the same budget.
   if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoadWarps) {
@@ -809,6 +882,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       err |= load_tiles(L, n_tiles, bar(B_KV_FULL), bar(B_KV_EMPTY), 0u, abort_flag,
                         a.error_word);
     }
+    if (rank == 1) epilogue((warp - kLoadWarp0) >> 2);
     finish();
     return;
   } else if (warp == kQWarp && rank == 0) {
@@ -1071,62 +1145,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(B_CORR_DONE));
     }
-    // epilogue: O / l, 64 columns at a time, through this warp's 8 KiB of the
-    // (now idle) stage region so that the global stores are whole rows
-    bool ok = wait_bar_all(bar(B_FINAL), 0, abort_flag, a.error_word) && n_tiles > 0;
-    const bool have_ml = wait_bar_all(bar(B_ML_FULL), 0, abort_flag, a.error_word, true);
-    ok = ok && have_ml;  // warp-uniform: gates the warp-collective TMEM loads below
-    tc_fence_after();
-    const float m = have_ml ? reinterpret_cast<const float*>(smem + OFF_ML)[h] : -INFINITY;
-    const float l = have_ml ? reinterpret_cast<const float*>(smem + OFF_ML + 512)[h] : 0.f;
-    const bool has_rows = ok && l > 0.f;  // per head (lane)
-    const float inv_l = has_rows ? 1.f / l : 0.f;
-    const float lse = has_rows ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    const uint32_t stg = sbase + OFF_STAGE + (uint32_t)wq * 8192u;
-    // One split: the bf16 output.  Several: this split's partial O / l in fp16
-    // (|O / l| is at most the largest |value|, which the loaders hold below
-    // 65536, so fp16 keeps it; 11 significant bits, against bf16's 8 in the
-    // final output) for the merge kernel.  Both are 16-bit: 64 B per head per
-    // 32 columns.
-    const bool partial = a.splits > 1;
-    uint16_t* dst = partial ? a.ws_o + (((int64_t)r * a.splits + split) * kHeads + wq * 32) * kDV
-                            : a.out + ((int64_t)r * a.H + wq * 32) * kDV;
-    for (int c0 = 0; c0 < kDV; c0 += 32) {  // 32 columns at a time (few live registers)
-      uint32_t u[32];
-      if (ok) {
-        const uint32_t oa = tm + lane_off + TM_O + c0;
-        tmem_ld16p(oa, u);
-        tmem_ld16p(oa + 16, u + 16);
-        tmem_ld_wait();
-      }
-      // a head's 32 columns are 4 chunks of 16 B, chunk k at k ^ (lane % 4)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x = __uint_as_float(u[8 * k + 2 * i]) * inv_l;
-          const float y = __uint_as_float(u[8 * k + 2 * i + 1]) * inv_l;
-          pk[i] = !has_rows ? 0u : partial ? pack_f16x2(x, y) : pack_bf16x2(x, y);
-        }
-        st_shared_v4(stg + lane * 64 + ((k ^ (lane & 3)) << 4),
-                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
-      }
-      __syncwarp();
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {  // 8 heads x 64 B per instruction
-        const int row = 8 * i + (lane >> 2), k = lane & 3;
-        const uint4 v = ld_shared_v4(stg + row * 64 + ((k ^ (row & 3)) << 4));
-        if (wq * 32 + row < a.H)
-          *reinterpret_cast<uint4*>(dst + (int64_t)row * kDV + c0 + 8 * k) = v;
-      }
-      __syncwarp();
-    }
-    if (a.splits == 1) {
-      if (h < a.H && a.lse) a.lse[(int64_t)r * a.H + h] = lse;
-    } else {
-      a.ws_lse[((int64_t)r * a.splits + split) * kHeads + h] = lse;
-    }
+    epilogue(2);
     finish();
     return;
   } else if (rank == 1 && !FP8 && warp == 2) {
