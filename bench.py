@@ -205,8 +205,8 @@ class ClockSampler:
         or more, and while it initialises the CUDA launches of the first timed
         steps ran up to ~10x slower.  A timed region of a few milliseconds holds
         no 100-ms sample of its own, so the record keeps the samples from here
-        on (the GPU has just run the warm-up) together with those taken during
-        the timed region."""
+        on (the warm-up runs next) together with those taken during the timed
+        region."""
         t0 = time.time()
         while self.proc is not None and self._lines() < 2 and time.time() - t0 < timeout_s:
             time.sleep(0.05)
@@ -569,18 +569,11 @@ def run_ours(args):
         if lib.hs_gather(ph, 0, pad.data_ptr(), R * K, gather_d.data_ptr(), sptr) != 0:
             raise RuntimeError("pre-load gather failed")
     pretouch_ms = pretouch_host_pool(torch, hs, pool)
-    torch.cuda.synchronize()
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    c0.record(stream)
-    step_fn(0)
-    c1.record(stream)
-    for t in range(1, args.warmup):
-        step_fn(t)
-    torch.cuda.synchronize()
-    cold_ms = c0.elapsed_time(c1) if args.warmup > 0 else None
-    cold_misses = int(cnt_d[0].sum().item()) if args.warmup > 0 else None
-    if dist is not None:
-        dist.barrier()
+    # The clock sampler starts, and the timing events are made, before the cold
+    # step and the warm-up, so that the timed region follows the warm-up with
+    # no more idle time than its synchronize: after an idle spell of a
+    # millisecond or more, the first steps measured 0.5-1.0 ms (then 0.3-0.4)
+    # against 0.27 ms in steady state.
     clocks = ClockSampler(local) if not args.profile else None
     if clocks:
         clocks.start()
@@ -592,6 +585,16 @@ def run_ours(args):
            for _ in range(n_ev)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    step_fn(0)
+    c1.record(stream)
+    for t in range(1, args.warmup):
+        step_fn(t)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
         step_fn(args.warmup + i, None if attention else evs[i])
@@ -599,6 +602,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     clock_info = clocks.stop() if clocks else None
     elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    cold_ms = c0.elapsed_time(c1) if args.warmup > 0 else None
+    cold_misses = int(cnt_d[0].sum().item()) if args.warmup > 0 else None
     misses_main = int(cnt_d[args.warmup:args.warmup + args.steps].sum().item())
     k0 = args.warmup + args.steps if attention else args.warmup
     if attention:
@@ -863,19 +868,21 @@ def run_mixed(args):
     h2d_peak = measure_h2d_peak(torch) if not args.profile else float("nan")
     d2h_peak = measure_d2h_peak(torch) if not args.profile else float("nan")
     pretouch_ms = pretouch_host_pool(torch, hs, pool)
-    for t in range(args.warmup):
-        one_step(t)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
+    # sampler and events before the warm-up: the timed region follows it with
+    # no idle time beyond its synchronize (see run_ours)
     clocks = ClockSampler(local) if not args.profile else None
     if clocks:
         clocks.start()
         clocks.wait_ready()
     evr = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for t in range(args.warmup):
+        one_step(t)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
     launches[0] = 0
     off_steps = [t for t in range(args.warmup, steps_total) if scen.appends[t]]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
@@ -1022,16 +1029,18 @@ def run_spec(args):
     peaks = load_peaks()
     h2d_peak = measure_h2d_peak(torch) if not args.profile else float("nan")
     pretouch_ms = pretouch_host_pool(torch, hs, pool)
-    for t in range(args.warmup):
-        fused_step(t)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
+    # sampler and events before the warm-up: the timed region follows it with
+    # no idle time beyond its synchronize (see run_ours)
     clocks = ClockSampler(local) if not args.profile else None
     if clocks:
         clocks.start()
         clocks.wait_ready()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for t in range(args.warmup):
+        fused_step(t)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
     torch.cuda.synchronize()
     t_start.record(stream)
     for i in range(args.steps):
