@@ -220,10 +220,13 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
 // list goes from host row src(i) to pool row dst(i) (dst < 0: skip).  Each
 // thread keeps kCopyUnroll 16-byte loads in flight before it stores them; the
 // addresses are formed again for the stores rather than held in registers.
-template <typename SrcF, typename DstF>
+// hook() runs once per thread while its first loads are in flight (or at the
+// end when it has none), for work that should overlap their latency.
+template <typename SrcF, typename DstF, typename HookF>
 __device__ __forceinline__ void copy_host_rows(const uint4* hsrc, uint4* kdst, int rv, int i_lo,
-                                               int i_hi, SrcF src, DstF dst) {
+                                               int i_hi, SrcF src, DstF dst, HookF hook) {
   const int total = (i_hi - i_lo) * rv;
+  bool hooked = false;
   for (int base = threadIdx.x; base < total; base += kThreads * kCopyUnroll) {
     uint4 v[kCopyUnroll];
 #pragma unroll
@@ -233,6 +236,10 @@ __device__ __forceinline__ void copy_host_rows(const uint4* hsrc, uint4* kdst, i
         const int i = i_lo + c / rv, e = c % rv;
         if (dst(i) >= 0) v[u] = __ldcs(hsrc + (int64_t)src(i) * rv + e);
       }
+    }
+    if (!hooked) {  // once, while the first loads are in flight
+      hook();
+      hooked = true;
     }
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
@@ -244,18 +251,19 @@ __device__ __forceinline__ void copy_host_rows(const uint4* hsrc, uint4* kdst, i
       }
     }
   }
+  if (!hooked) hook();
 }
 
-// Host rows 0 .. n-1 of a list -> shared-memory staging (row i at stage +
-// i * rv * 16), kCopyUnroll 16-byte loads in flight per thread.  (Vector loads
+// Host rows i_lo .. i_hi-1 of a list -> shared-memory staging (row i at stage
+// + i * rv * 16), kCopyUnroll 16-byte loads in flight per thread.  (Vector loads
 // through registers: asynchronous cp.async copies from mapped host memory keep
 // far fewer reads in flight per SM.)
 template <typename SrcF>
 __device__ __forceinline__ void stage_host_rows(const uint4* hsrc, unsigned char* stage, int rv,
-                                                int n, SrcF src) {
+                                                int i_lo, int i_hi, SrcF src) {
   uint4* st = reinterpret_cast<uint4*>(stage);
-  const int total = n * rv;
-  for (int base = threadIdx.x; base < total; base += kThreads * kCopyUnroll) {
+  const int total = i_hi * rv;
+  for (int base = i_lo * rv + (int)threadIdx.x; base < total; base += kThreads * kCopyUnroll) {
     uint4 v[kCopyUnroll];
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
@@ -299,9 +307,11 @@ __device__ __forceinline__ void unstage_rows(const unsigned char* stage, uint4* 
 // phases: (1) each fetch CTA tells CTA 0 it has read the position -> slot
 // array, which CTA 0 updates only after all have; (2) CTA 0 tells each fetch
 // CTA that every miss's row id is written, which says where its staged rows
-// go.  A fetch CTA waits for CTA 0 alone, never for another fetch CTA.  Rows
-// beyond a CTA's staging capacity are copied straight from host memory to
-// their slots after (2).  With C == 1, CTA 0 starts the host reads of a first
+// go.  A fetch CTA waits for CTA 0 alone, never for another fetch CTA.  It
+// stages rows only until (2) has arrived (checked after each round of loads)
+// or its staging is full; the rest of its misses go straight from host memory
+// to their slots after (2), the staged rows being written out while the first
+// of those loads are in flight.  With C == 1, CTA 0 starts the host reads of a first
 // small batch (one 16-byte load per thread, held in registers) before it
 // chooses victims.
 template <int P_CT, int RV_CT>
@@ -394,8 +404,22 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     __syncthreads();
     // (1) this CTA is done reading the position -> slot array
     if (tid == 0) hs_ptx::mbar_arrive_remote(hs_ptx::mapa(my_bar, 0));
-    const int n_stage = min(n_local, cap);
-    stage_host_rows(hsrc, smem + fp.stage, rv, n_stage, [&](int i) { return f_p[i]; });
+    // Host rows go to shared-memory staging one round of loads at a time
+    // (kCopyUnroll per thread) only until CTA 0 has written the row ids (or the
+    // staging is full); the rest go straight to their slots afterwards.
+    int n_stage = 0;
+    int* s_go = s_warp + kWarps + 1;
+    for (;;) {
+      const int n_next = min(n_local, min(cap, n_stage + kThreads * kCopyUnroll / rv));
+      if (n_next <= n_stage) break;
+      stage_host_rows(hsrc, smem + fp.stage, rv, n_stage, n_next, [&](int i) { return f_p[i]; });
+      n_stage = n_next;
+      if (tid == 0) *s_go = hs_ptx::mbar_test_wait_cluster(my_bar, 0) ? 1 : 0;
+      __syncthreads();
+      const bool go = *s_go != 0;
+      __syncthreads();  // before thread 0 writes s_go again
+      if (go) break;
+    }
     // (2) CTA 0 has written the row id of every miss
     int* s_ok = s_warp + kWarps;
     if (tid < 32) {  // the whole warp polls, so that it sees the phase at once
@@ -407,9 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     if (ok) {
       for (int i = tid; i < n_local; i += kThreads) f_dst[i] = __ldcg(out + f_j[i]);
       __syncthreads();
-      unstage_rows(smem + fp.stage, kdst, rv, n_stage, [&](int i) { return f_dst[i]; });
       copy_host_rows(hsrc, kdst, rv, n_stage, n_local, [&](int i) { return f_p[i]; },
-                     [&](int i) { return f_dst[i]; });
+                     [&](int i) { return f_dst[i]; }, [&] {
+                       unstage_rows(smem + fp.stage, kdst, rv, n_stage,
+                                    [&](int i) { return f_dst[i]; });
+                     });
     } else if (tid == 0) {
       atomicOr(a.error_word, HS_DEV_ERR_WAIT);
     }
@@ -649,7 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1) resolve_kernel(const ResolveArgs 
     const int32_t row = slot_row(i);
     if (row >= 0) kdst[(int64_t)row * rv + e] = early_v;
   }
-  copy_host_rows(hsrc, kdst, rv, n_early, n_serve, [&](int i) { return s_miss_p[i]; }, slot_row);
+  copy_host_rows(hsrc, kdst, rv, n_early, n_serve, [&](int i) { return s_miss_p[i]; }, slot_row,
+                 [] {});
 }
 
 // Self-test of wait_peer_bar's time limit: one thread waits on a barrier of
