@@ -24,3 +24,36 @@ def test_oracle_sample_on_both_row_formats():
         rows, secs, steps = bench.oracle_sample(w, seconds=1e9, units=1, steps_cap=3, skip=1,
                                                 fp8=fp8)
         assert steps == 2 and rows == 2 * w.K and secs > 0
+
+
+def test_clock_sampler_summarises_samples_and_throttle_reasons(tmp_path):
+    """The clocks record: median SM clock under load, the maximum, and every
+    throttle reason seen Active (from nvidia-smi's CSV, here written by hand)."""
+    import bench
+
+    class _Done:  # stands in for the nvidia-smi process
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    csv = tmp_path / "clocks.csv"
+    csv.write_text(
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+        "0, 1980, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active\n"
+        "0, 2070, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+        "garbled line\n")
+    s = bench.ClockSampler(0)
+    s.proc, s.path = _Done(), str(csv)
+    rec = s.stop()
+    assert rec == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 3,
+                   "reasons": ["sw_power_cap"]}
+    assert not csv.exists()  # the sample file is removed
+
+
+def test_clock_sampler_without_nvidia_smi_says_so():
+    import bench
+    s = bench.ClockSampler(0)
+    s.wait_ready(timeout_s=0.01)  # no process: returns at once (plus its short settle)
+    assert s.stop() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
